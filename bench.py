@@ -1,0 +1,507 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 gated delta rule (GDR) recurrence.
+
+One JSON line on stdout (rank 0).  The headline workload is the Qwen3.5-shaped
+decode step: batch 256 rows x 1 token (8 padding rows), nk=16, nv=32,
+K=V=128, float32 per-token inputs, bf16 state pool [512, 32, 128, 128] read
+and written in place.  `value` is head-tokens/s (live tokens x nv per step /
+step time) with inputs resident in HBM; `e2e` is the same metric through the
+public Python API with the step's inputs copied from pinned host memory and
+the output copied back inside the timed region.  The L2 cache is flushed
+(a 2x-L2 memset) before every timed step.
+
+Secondary workloads (ragged prefill, verify + fold, Gated Delta Product
+snapshots + rollback) are timed the same way and reported under "secondary".
+
+--impl reference times the CPU oracle (oracle/, float64 C loops, one thread)
+on the same decode workload and metric.
+
+Multi-GPU (torchrun): every rank runs its own decode batch on its own GPU (the
+rows of a batch are independent, so the shards exchange nothing); value is the
+head-tokens of all ranks over the slowest rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN recurrence head-tokens/s (decode, verify+fold); achieved HBM GB/s vs peak"
+UNIT = "head-tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gdr", choices=["gdr", "reference"])
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=1.0,
+                    help="seconds of untimed steps after warm-up (steady clocks)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers ---
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_deltanet_linear_gdr_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else null)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel_key]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = (uuid or "").lower().replace("gpu-", "")
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            if self.uuid and self.uuid not in f[1].lower().replace("gpu-", ""):
+                continue
+            try:
+                rows.append((float(f[2]), float(f[3]), f[6:10]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------- workloads ---
+
+def decode_bytes(w, sb):
+    """Algorithmic HBM bytes of one decode/forward call."""
+    conv = 2 * w.nk * w.K + w.nv * w.V
+    live = w.slot_idx >= 0
+    L = w.row_lengths
+    live_tok = int(L[live].sum())
+    pad_tok = int(L[~live].sum())
+    live_rows = int(((L > 0) & live).sum())
+    state = live_rows * w.nv * w.K * w.V * sb * 2
+    act = live_tok * (conv + 2 * w.nv + w.nv * w.V) * 4 + pad_tok * w.nv * w.V * 4
+    idx = w.batch * 4 + (w.batch + 1) * 4
+    return state + act + idx
+
+
+def fma_ops(head_tokens, K, V, per=4):
+    return head_tokens * per * K * V
+
+
+# ------------------------------------------------------------- GPU side ---
+
+class DecodeStep:
+    """Device-resident decode workload plus pinned host copies for e2e."""
+
+    def __init__(self, w, dev):
+        import numpy as np
+        import torch
+        self.w = w
+        self.dev = dev
+        self.h = {
+            "qkv": torch.from_numpy(w.qkv).pin_memory(),
+            "decay": torch.from_numpy(w.decay).pin_memory(),
+            "beta": torch.from_numpy(w.beta).pin_memory(),
+            "slot": torch.from_numpy(w.slot_idx).pin_memory(),
+            "off": torch.from_numpy(w.offsets).pin_memory(),
+        }
+        self.d = {k: v.to(dev) for k, v in self.h.items()}
+        pool = w.state_pool()
+        self.state = torch.from_numpy(pool.view(np.int16)).to(dev).view(torch.bfloat16) \
+            if pool.dtype == np.uint16 else torch.from_numpy(pool).to(dev)
+        del pool
+        self.out = torch.empty((w.total_tokens, w.nv * w.V), dtype=torch.float32, device=dev)
+        self.h_out = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.h.values())
+        self.d2h_bytes = self.out.numel() * 4
+
+    def run(self):
+        import gated_deltanet_linear_gdr_gb300 as gdr
+        d = self.d
+        gdr.gdr_fwd(d["qkv"], d["decay"], d["beta"], self.state, d["slot"], d["off"],
+                    out=self.out, max_row_len=1)
+
+    def run_e2e(self):
+        import gated_deltanet_linear_gdr_gb300 as gdr
+        d, h = self.d, self.h
+        for k in d:
+            d[k].copy_(h[k], non_blocking=True)
+        gdr.gdr_fwd(d["qkv"], d["decay"], d["beta"], self.state, d["slot"], d["off"],
+                    out=self.out, max_row_len=1)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+
+def time_steps(fn, steps, flush, stream):
+    """Per-step CUDA-event durations (ms) on `stream`, L2 flushed before each."""
+    import torch
+    evs = []
+    for _ in range(steps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def secondary(dev, flush, stream, hbm_peak, steps):
+    """Prefill, verify+fold and GDP snapshot+rollback workloads, timed like decode."""
+    import numpy as np
+    import torch
+    import gated_deltanet_linear_gdr_gb300 as gdr
+    from gated_deltanet_linear_gdr_gb300 import workloads as W
+    props = torch.cuda.get_device_properties(dev)
+    res = {}
+
+    def t(x):
+        return torch.from_numpy(x).to(dev)
+
+    def pool_dev(w):
+        pool = w.state_pool(w.live_slots())
+        if pool.dtype == np.uint16:
+            return torch.from_numpy(pool.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(pool).to(dev)
+
+    # --- ragged prefill (FP32-FMA bound)
+    w = W.prefill()
+    st = pool_dev(w)
+    qkv, dec, bet, slot, off = t(w.qkv), t(w.decay), t(w.beta), t(w.slot_idx), t(w.offsets)
+    out = torch.empty((w.total_tokens, w.nv * w.V), device=dev)
+    fn = lambda: gdr.gdr_fwd(qkv, dec, bet, st, slot, off, out=out)  # noqa: E731
+    for _ in range(2):
+        fn()
+    ms = statistics.median(time_steps(fn, max(3, steps // 10), flush, stream))
+    ht = w.live_head_tokens
+    clk = props.clock_rate * 1e3 if hasattr(props, "clock_rate") else 2.07e9
+    fp32_peak = props.multi_processor_count * 128 * clk
+    res["prefill"] = {
+        "workload": f"ragged prefill: {w.batch} rows, lengths {w.row_lengths.min()}..{w.row_lengths.max()}"
+                    f" (T={w.total_tokens}), nk=16, nv=32, K=V=128, bf16 pool [16,32,128,128]",
+        "ms": ms, "head_tokens_per_s": ht / (ms * 1e-3),
+        "fma_tflops_equiv": fma_ops(ht, w.K, w.V) / (ms * 1e-3) / 1e12,
+        "fp32_fma_peak_tops": fp32_peak / 1e12,
+        "frac_fp32_fma": fma_ops(ht, w.K, w.V) / (ms * 1e-3) / fp32_peak,
+        "hbm_gbs": decode_bytes(w, 2) / (ms * 1e-3) / 1e9,
+    }
+    del st, qkv, dec, bet, out
+
+    # --- speculative verify + fold (bf16 pool, fp32 ring)
+    w = W.verify_fold()
+    st = pool_dev(w)
+    qkv, dec, bet, slot, off = t(w.qkv), t(w.decay), t(w.beta), t(w.slot_idx), t(w.offsets)
+    stride = (gdr.gdr_ring_record_elements(w.K, w.V, w.nv // w.nk) + 3) // 4 * 4
+    ring = torch.zeros((w.ring_rows, w.nk, w.ring_len, stride), device=dev)
+    rsi, cnt = t(w.ring_slot_idx), t(w.counts)
+    out = torch.empty((w.total_tokens, w.nv * w.V), device=dev)
+    v_fn = lambda: gdr.gdr_verify_ring(qkv, dec, bet, st, slot, off, ring, rsi, out=out)  # noqa
+    f_fn = lambda: gdr.gdr_fold(st, slot, ring, rsi, cnt)  # noqa: E731
+    for _ in range(2):
+        v_fn(); f_fn()  # noqa: E702
+    tv = statistics.median(time_steps(v_fn, steps, flush, stream))
+    tf = statistics.median(time_steps(f_fn, steps, flush, stream))
+    L = w.row_lengths
+    short = L <= w.ring_len
+    rec = w.K + ((w.nv // w.nk + 3) // 4) * 4 + (w.nv // w.nk) * w.V
+    conv = 2 * w.nk * w.K + w.nv * w.V
+    vbytes = (w.batch * w.nv * w.K * w.V * 2 + int((~short).sum()) * w.nv * w.K * w.V * 2
+              + w.total_tokens * (conv + 2 * w.nv + w.nv * w.V) * 4
+              + int(L[short].sum()) * w.nk * rec * 4)
+    active = (w.counts > 0) & (w.counts <= w.ring_len) & (w.slot_idx >= 0)
+    fbytes = (int(active.sum()) * w.nv * w.K * w.V * 2 * 2
+              + int(w.counts[active].sum()) * w.nk * rec * 4)
+    ht = w.live_head_tokens
+    res["verify_fold"] = {
+        "workload": "verify: 127 rows x 5 drafts + 1 row of 12, RING_LEN 8, nk=16, nv=32, "
+                    "K=V=128, bf16 pool [256,32,128,128], fp32 ring [256,16,8,388]; then fold "
+                    "of accepted counts ~U{0..5}",
+        "verify_ms": tv, "fold_ms": tf, "head_tokens_per_s": ht / ((tv + tf) * 1e-3),
+        "verify_hbm_gbs": vbytes / (tv * 1e-3) / 1e9, "fold_hbm_gbs": fbytes / (tf * 1e-3) / 1e9,
+        "frac_hbm_verify_plus_fold": (vbytes + fbytes) / ((tv + tf) * 1e-3) / 1e9 / hbm_peak,
+    }
+    del st, ring, qkv, out
+
+    # --- GDP snapshots + rollback (fp32 cache)
+    w = W.gdp_snapshots()
+    st = pool_dev(w)
+    qkv, dec, bet, slot, off = t(w.qkv), t(w.decay), t(w.beta), t(w.slot_idx), t(w.offsets)
+    inter = torch.zeros((w.max_slots, w.n_inter, w.nv, w.K, w.V), device=dev)
+    acc = t(w.accepted)
+    out = torch.empty((w.total_tokens, w.nv * w.V), device=dev)
+    s_fn = lambda: gdr.gdr_fwd_snapshots(qkv, dec, bet, st, slot, off, inter, w.steps_per_token,  # noqa
+                                         out=out, decay_is_log=True)
+    r_fn = lambda: gdr.gdr_rollback(st, slot, inter, acc)  # noqa: E731
+    for _ in range(2):
+        s_fn(); r_fn()  # noqa: E702
+    ts = statistics.median(time_steps(s_fn, steps, flush, stream))
+    tr = statistics.median(time_steps(r_fn, steps, flush, stream))
+    sbytes = decode_bytes(w, 4) + w.batch * w.n_inter * w.nv * w.K * w.V * 4
+    rbytes = w.batch * w.nv * w.K * w.V * 4 * 2
+    ht = w.live_head_tokens
+    res["gdp_snapshots"] = {
+        "workload": "GDP spec-decode: 64 requests x 4 drafts x 2 Householder copies (T=8 each), "
+                    "spt=2, nk=16, nv=32, K=V=128, fp32 cache [128,32,128,128], "
+                    "intermediate [128,4,32,128,128]; then rollback",
+        "snapshots_ms": ts, "rollback_ms": tr, "head_tokens_per_s": ht / (ts * 1e-3),
+        "snapshots_hbm_gbs": sbytes / (ts * 1e-3) / 1e9, "rollback_hbm_gbs": rbytes / (tr * 1e-3) / 1e9,
+        "frac_hbm_snapshots": sbytes / (ts * 1e-3) / 1e9 / hbm_peak,
+        "frac_hbm_rollback": rbytes / (tr * 1e-3) / 1e9 / hbm_peak,
+    }
+    del st, inter, qkv, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline_decode(w, budget_s=10.0):
+    """The CPU oracle (float64 C loops, one thread) on whole decode batches."""
+    import oracle
+    pool = w.state_pool(w.live_slots())
+    reps, t_total = 0, 0.0
+    while t_total < budget_s and reps < 100:
+        p = oracle.Problem(w.qkv, w.decay, w.beta, pool.copy(), w.slot_idx, w.offsets,
+                           nk=w.nk, nv=w.nv, K=w.K, V=w.V)
+        t0 = time.perf_counter()
+        oracle.fwd(p)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return {"value": w.live_head_tokens * reps / t_total, "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{reps} whole decode batches (256 rows, {w.live_head_tokens} live "
+                      f"head-tokens each), float64 C loops, single thread, {t_total:.1f} s"}
+
+
+def run_gdr(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import gated_deltanet_linear_gdr_gb300 as gdr
+    from gated_deltanet_linear_gdr_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    gdr.load_library()
+    stream = torch.cuda.current_stream(dev)
+
+    w = W.decode(seed=1 + rank)
+    step = DecodeStep(w, dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20)
+    flush_buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    hbm_peak, peak_kind = peaks()
+    uuid = str(getattr(props, "uuid", "")) or None
+    sampler = ClockSampler(uuid)
+
+    for _ in range(max(3, args.warmup)):
+        flush()
+        step.run()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_end = time.time() + args.soak_s
+    while time.time() < t_end:
+        for _ in range(20):
+            flush()
+            step.run()
+        torch.cuda.synchronize()
+
+    # ---- timed region: exactly `steps` steps
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    per = time_steps(step.run, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    st = gdr.gdr_get_status(clear=True)
+    if st:
+        raise RuntimeError(f"device status after timed region: {gdr.status_names(st)}")
+
+    kernel_ms = sum(per)
+    t_max = torch.tensor([kernel_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    kernel_ms_max = float(t_max.item())
+    ms_per_step = kernel_ms_max / args.steps
+    ht = w.live_head_tokens
+    value = ht * world * args.steps / (kernel_ms_max * 1e-3)
+
+    # ---- end-to-end through the public API with host buffers
+    for _ in range(3):
+        step.run_e2e()
+    torch.cuda.synchronize()
+    per_e2e = time_steps(step.run_e2e, args.steps, flush, stream)
+    e2e_ms = torch.tensor([sum(per_e2e)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_value = ht * world * args.steps / (float(e2e_ms.item()) * 1e-3)
+
+    alg_bytes = decode_bytes(w, 2)
+    achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": "decode: batch 256 rows x 1 token (248 live, 8 padding slot -1), nk=16, "
+                        "nv=32, K=V=128, fp32 q/k/v/decay/beta, bf16 state pool "
+                        "[512,32,128,128] at random slots",
+            "global_batch": 256 * world, "seq_len": 1, "parallelism": f"dp{world}",
+            "l2": "flushed before every timed step (memset of 2x L2)",
+            "head_tokens_per_step": ht * world,
+            "alg_bytes_per_step": alg_bytes,
+            "timed_wall_s": wall,
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "gdr::k_decode<bf16,128>", "achieved": achieved,
+            "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+            "peak_kind": f"{peak_kind} (STREAM-style copy)",
+            "traffic": ncu_traffic("k_decode_bf16_128"),
+        },
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": step.h2d_bytes,
+                "d2h_bytes_per_step": step.d2h_bytes},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_secondary:
+        try:
+            line["secondary"] = secondary(dev, flush, stream, hbm_peak, max(5, args.steps // 2))
+        except Exception as e:  # report, never hide
+            line["secondary"] = {"error": repr(e)}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle as it stands, on the decode workload (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from gated_deltanet_linear_gdr_gb300 import workloads as W
+    w = W.decode()
+    pool = w.state_pool(w.live_slots())
+
+    def one():
+        p = oracle.Problem(w.qkv, w.decay, w.beta, pool.copy(), w.slot_idx, w.offsets,
+                           nk=w.nk, nv=w.nv, K=w.K, V=w.V)
+        t0 = time.perf_counter()
+        oracle.fwd(p)
+        return time.perf_counter() - t0
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    times = [one() for _ in range(args.steps)]
+    total = sum(times)
+    ht = w.live_head_tokens
+    value = ht * args.steps / total
+    sample = (f"whole decode batch per step (256 rows, {ht} live head-tokens), float64 C loops, "
+              f"single thread")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": "decode: batch 256 rows x 1 token (248 live, 8 padding slot -1), "
+                               "nk=16, nv=32, K=V=128, bf16 state pool [512,32,128,128]",
+                   "global_batch": 256, "seq_len": 1, "parallelism": "none (CPU oracle)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gdr(args)
+
+
+if __name__ == "__main__":
+    main()

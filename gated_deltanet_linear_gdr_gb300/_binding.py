@@ -1,0 +1,291 @@
+"""Thin ctypes binding over libgdr.so (include/gdr.h).
+
+Argument marshalling only: tensors are checked for dtype/device/shape, their
+data pointers and strides are packed into gdr_step_args, and the C entry point
+of the same name runs every step of the path on the GPU.  PyTorch supplies the
+device memory and the current stream; nothing here computes.
+
+If libgdr.so is missing the first call raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdr.so")
+
+GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_CUDA = 0, -1, -2, -3
+GDR_F32, GDR_BF16 = 0, 1
+STATUS_BITS = {
+    0x1: "BAD_SLOT", 0x2: "BAD_OFFSETS", 0x4: "BAD_RING_SLOT", 0x8: "BAD_COUNT",
+    0x10: "ROW_TOO_LONG", 0x20: "BAD_ACCEPTED", 0x40: "SNAPSHOT_OVERFLOW",
+}
+
+
+class GdrError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"gdr error {code}: {msg}")
+        self.code = code
+
+
+class gdr_step_args(ctypes.Structure):
+    """Mirror of struct gdr_step_args in include/gdr.h (same order and types)."""
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("nv", ctypes.c_int32), ("nk", ctypes.c_int32),
+        ("K", ctypes.c_int32), ("V", ctypes.c_int32),
+        ("decay_is_log", ctypes.c_int32), ("use_qk_l2norm", ctypes.c_int32),
+        ("state_dtype", ctypes.c_int32),
+        ("total_tokens", ctypes.c_int64), ("max_row_len", ctypes.c_int64),
+        ("qkv", ctypes.c_void_p), ("qkv_seq_stride", ctypes.c_int64),
+        ("qkv_chan_stride", ctypes.c_int64),
+        ("decay", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+        ("tok_seq_stride", ctypes.c_int64), ("tok_head_stride", ctypes.c_int64),
+        ("scale", ctypes.c_float), ("eps", ctypes.c_float),
+        ("out", ctypes.c_void_p), ("out_seq_stride", ctypes.c_int64),
+        ("out_vdim_stride", ctypes.c_int64),
+        ("state", ctypes.c_void_p), ("state_slot_stride", ctypes.c_int64),
+        ("state_head_stride", ctypes.c_int64), ("state_kdim_stride", ctypes.c_int64),
+        ("state_vdim_stride", ctypes.c_int64), ("max_slots", ctypes.c_int64),
+        ("slot_idx", ctypes.c_void_p), ("offsets", ctypes.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libgdr.so (built by gated_deltanet_linear_gdr_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"{p} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                    f"g.build()\"` (the GDR path has no CPU or Python fallback)")
+            lib = ctypes.CDLL(p)
+            A = ctypes.POINTER(gdr_step_args)
+            vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            sig = {
+                "gdr_last_error": ([], ctypes.c_char_p),
+                "gdr_version": ([], ctypes.c_int),
+                "gdr_output_shape": ([i64, i32, i32, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+                "gdr_ring_record_elements": ([i32, i32, i32], ctypes.c_int),
+                "gdr_fwd": ([A, vp], ctypes.c_int),
+                "gdr_verify_ring": ([A, vp, i32, i64, i32, i64, vp, vp], ctypes.c_int),
+                "gdr_fold": ([A, vp, i32, i64, i32, i64, vp, vp, vp], ctypes.c_int),
+                "gdr_fwd_snapshots": ([A, vp, i64, i64, i64, i32, i32, vp], ctypes.c_int),
+                "gdr_rollback": ([A, vp, i64, i64, i64, i32, vp, vp], ctypes.c_int),
+                "gdr_get_status": ([ctypes.POINTER(ctypes.c_uint32), i32], ctypes.c_int),
+            }
+            for name, (args, res) in sig.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            if path is None:
+                _lib = lib
+            else:
+                return lib
+    return _lib
+
+
+def _check(rc: int):
+    if rc != GDR_OK:
+        msg = load_library().gdr_last_error().decode(errors="replace")
+        raise GdrError(rc, msg)
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    return t
+
+
+def _state_dtype(state: torch.Tensor) -> int:
+    if state.dtype == torch.bfloat16:
+        return GDR_BF16
+    if state.dtype == torch.float32:
+        return GDR_F32
+    raise TypeError(f"state dtype {state.dtype}: expected bfloat16 or float32")
+
+
+def make_args(qkv, decay, beta, state, slot_idx, offsets, out, *, nk: int,
+              decay_is_log=False, use_qk_l2norm=True, scale=0.0, eps=1e-6,
+              max_row_len=0) -> gdr_step_args:
+    """Pack tensors into gdr_step_args (no copies; strides passed through)."""
+    _dev(state, "state", (torch.bfloat16, torch.float32))
+    if state.dim() != 4:
+        raise ValueError("state must be [max_slots, nv, K, V]")
+    max_slots, nv, K, V = state.shape
+    _dev(slot_idx, "slot_idx", torch.int32)
+    batch = slot_idx.shape[0]
+    a = gdr_step_args()
+    a.batch, a.nv, a.nk, a.K, a.V = batch, nv, nk, K, V
+    a.decay_is_log, a.use_qk_l2norm = int(bool(decay_is_log)), int(bool(use_qk_l2norm))
+    a.state_dtype = _state_dtype(state)
+    a.max_row_len = int(max_row_len)
+    a.scale, a.eps = float(scale), float(eps)
+    a.state = state.data_ptr()
+    (a.state_slot_stride, a.state_head_stride, a.state_kdim_stride,
+     a.state_vdim_stride) = state.stride()
+    a.max_slots = max_slots
+    a.slot_idx = slot_idx.data_ptr()
+    if qkv is not None:
+        _dev(qkv, "qkv", torch.float32)
+        _dev(decay, "decay", torch.float32)
+        _dev(beta, "beta", torch.float32)
+        _dev(out, "out", torch.float32)
+        _dev(offsets, "offsets", torch.int32)
+        T = qkv.shape[0]
+        if qkv.shape[1] != 2 * nk * K + nv * V:
+            raise ValueError(f"qkv has {qkv.shape[1]} channels, expected 2*nk*K + nv*V = "
+                             f"{2 * nk * K + nv * V}")
+        if decay.shape != (T, nv) or beta.shape != (T, nv) or decay.stride() != beta.stride():
+            raise ValueError("decay and beta must both be [T, nv] with the same strides")
+        if out.shape != (T, nv * V):
+            raise ValueError(f"out must be [T, nv*V] = [{T}, {nv * V}]")
+        if offsets.shape != (batch + 1,) or not offsets.is_contiguous():
+            raise ValueError("offsets must be a contiguous [batch+1] int32 tensor")
+        a.total_tokens = T
+        a.qkv = qkv.data_ptr()
+        a.qkv_seq_stride, a.qkv_chan_stride = qkv.stride()
+        a.decay, a.beta = decay.data_ptr(), beta.data_ptr()
+        a.tok_seq_stride, a.tok_head_stride = decay.stride()
+        a.out = out.data_ptr()
+        a.out_seq_stride, a.out_vdim_stride = out.stride()
+        a.offsets = offsets.data_ptr()
+    if not slot_idx.is_contiguous():
+        raise ValueError("slot_idx must be contiguous")
+    return a
+
+
+def _nk_from_qkv(qkv, state):
+    nv, K, V = state.shape[1:]
+    rest = qkv.shape[1] - nv * V
+    if rest <= 0 or rest % (2 * K):
+        raise ValueError("cannot infer nk from qkv channels")
+    return rest // (2 * K)
+
+
+def gdr_output_shape(total_tokens: int, nv: int, V: int):
+    shp = (ctypes.c_int64 * 2)()
+    _check(load_library().gdr_output_shape(total_tokens, nv, V, shp))
+    return int(shp[0]), int(shp[1])
+
+
+def gdr_ring_record_elements(K: int, V: int, ratio: int) -> int:
+    n = load_library().gdr_ring_record_elements(K, V, ratio)
+    if n < 0:
+        _check(n)
+    return n
+
+
+def gdr_fwd(qkv, decay, beta, state, slot_idx, offsets, out=None, *, decay_is_log=False,
+            use_qk_l2norm=True, scale=0.0, eps=1e-6, max_row_len=0):
+    """Forward pass ("gated_delta_recurrence_fwd_gpu"); state updated in place; returns out."""
+    if out is None:
+        out = torch.empty(gdr_output_shape(qkv.shape[0], state.shape[1], state.shape[3]),
+                          dtype=torch.float32, device=qkv.device)
+    a = make_args(qkv, decay, beta, state, slot_idx, offsets, out, nk=_nk_from_qkv(qkv, state),
+                  decay_is_log=decay_is_log, use_qk_l2norm=use_qk_l2norm, scale=scale, eps=eps,
+                  max_row_len=max_row_len)
+    _check(load_library().gdr_fwd(ctypes.byref(a), _stream(qkv.device)))
+    return out
+
+
+def gdr_verify_ring(qkv, decay, beta, state, slot_idx, offsets, ring, ring_slot_idx, out=None, *,
+                    decay_is_log=False, use_qk_l2norm=True, scale=0.0, eps=1e-6, max_row_len=0):
+    """Verify pass ("gated_delta_recurrence_verify_ring_gpu"); ring is
+    [ring_rows, nk, ring_len, record_stride] float32 (dense)."""
+    _dev(ring, "ring", torch.float32)
+    _dev(ring_slot_idx, "ring_slot_idx", torch.int32)
+    if ring.dim() != 4 or not ring.is_contiguous():
+        raise ValueError("ring must be a contiguous [ring_rows, nk, ring_len, record_stride] tensor")
+    if out is None:
+        out = torch.empty(gdr_output_shape(qkv.shape[0], state.shape[1], state.shape[3]),
+                          dtype=torch.float32, device=qkv.device)
+    nk = _nk_from_qkv(qkv, state)
+    if ring.shape[1] != nk:
+        raise ValueError("ring.shape[1] must equal nk")
+    a = make_args(qkv, decay, beta, state, slot_idx, offsets, out, nk=nk, decay_is_log=decay_is_log,
+                  use_qk_l2norm=use_qk_l2norm, scale=scale, eps=eps, max_row_len=max_row_len)
+    _check(load_library().gdr_verify_ring(ctypes.byref(a), ring.data_ptr(), GDR_F32, ring.shape[0],
+                                          ring.shape[2], ring.shape[3], ring_slot_idx.data_ptr(),
+                                          _stream(qkv.device)))
+    return out
+
+
+def gdr_fold(state, slot_idx, ring, ring_slot_idx, counts):
+    """Fold the first counts[b] records of each row into its slot (in place)."""
+    _dev(ring, "ring", torch.float32)
+    _dev(ring_slot_idx, "ring_slot_idx", torch.int32)
+    _dev(counts, "counts", torch.int32)
+    if ring.dim() != 4 or not ring.is_contiguous():
+        raise ValueError("ring must be a contiguous [ring_rows, nk, ring_len, record_stride] tensor")
+    a = make_args(None, None, None, state, slot_idx, None, None, nk=ring.shape[1])
+    _check(load_library().gdr_fold(ctypes.byref(a), ring.data_ptr(), GDR_F32, ring.shape[0],
+                                   ring.shape[2], ring.shape[3], ring_slot_idx.data_ptr(),
+                                   counts.data_ptr(), _stream(state.device)))
+
+
+def _inter_strides(inter, state):
+    if inter.dtype != state.dtype:
+        raise TypeError("intermediate_states must have the pool's dtype")
+    if inter.dim() != 5 or inter.shape[2:] != state.shape[1:]:
+        raise ValueError("intermediate_states must be [slots, n_inter, nv, K, V]")
+    K, V = state.shape[2:]
+    if inter.stride(4) != 1 or inter.stride(3) != V:
+        raise ValueError("each [K, V] block of intermediate_states must be dense")
+    return inter.stride(0), inter.stride(1), inter.stride(2), inter.shape[1]
+
+
+def gdr_fwd_snapshots(qkv, decay, beta, state, slot_idx, offsets, inter, steps_per_token, out=None,
+                      *, decay_is_log=False, use_qk_l2norm=True, scale=0.0, eps=1e-6,
+                      max_row_len=0):
+    """Forward pass + snapshots ("core.ssm.ops.gdp.fused_recurrent", intermediate_states)."""
+    _dev(inter, "intermediate_states")
+    ss, st, sh, n_inter = _inter_strides(inter, state)
+    if out is None:
+        out = torch.empty(gdr_output_shape(qkv.shape[0], state.shape[1], state.shape[3]),
+                          dtype=torch.float32, device=qkv.device)
+    a = make_args(qkv, decay, beta, state, slot_idx, offsets, out, nk=_nk_from_qkv(qkv, state),
+                  decay_is_log=decay_is_log, use_qk_l2norm=use_qk_l2norm, scale=scale, eps=eps,
+                  max_row_len=max_row_len)
+    _check(load_library().gdr_fwd_snapshots(ctypes.byref(a), inter.data_ptr(), ss, st, sh,
+                                            n_inter, int(steps_per_token), _stream(qkv.device)))
+    return out
+
+
+def gdr_rollback(state, slot_idx, inter, accepted):
+    """state[slot] <- intermediate_states[slot, accepted[b]] (in place)."""
+    _dev(inter, "intermediate_states")
+    _dev(accepted, "accepted", torch.int32)
+    ss, st, sh, n_inter = _inter_strides(inter, state)
+    a = make_args(None, None, None, state, slot_idx, None, None, nk=1)
+    _check(load_library().gdr_rollback(ctypes.byref(a), inter.data_ptr(), ss, st, sh, n_inter,
+                                       accepted.data_ptr(), _stream(state.device)))
+
+
+def gdr_get_status(clear: bool = True) -> int:
+    """Device status word (GDR_STATUS_* bits); synchronises the device."""
+    v = ctypes.c_uint32(0)
+    _check(load_library().gdr_get_status(ctypes.byref(v), int(bool(clear))))
+    return int(v.value)
+
+
+def status_names(bits: int):
+    return [n for b, n in STATUS_BITS.items() if bits & b]

@@ -1,0 +1,348 @@
+// C ABI of libgdr.so: argument validation, lowering to kernel parameters and
+// dispatch.  Every check runs on the host before anything is launched; the
+// only device state the library owns is the per-device status word below.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "gdr_internal.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int ok() {
+    g_err.clear();
+    return GDR_OK;
+}
+
+// Sticky error bits set by kernels (GDR_STATUS_*), one word per device.
+__device__ unsigned int g_gdr_status;
+
+std::mutex g_status_mu;
+unsigned *g_status_ptr[64];
+
+// Device address of this device's status word (cached; host-side symbol names
+// are not device addresses).
+int status_ptr(unsigned **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(GDR_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_gdr_status);
+        if (e != cudaSuccess)
+            return fail(GDR_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+        g_status_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    *out = g_status_ptr[dev];
+    return GDR_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_dim(int K) { return K == 16 || K == 32 || K == 64 || K == 128; }
+
+int esize(int dtype) { return dtype == GDR_BF16 ? 2 : 4; }
+
+// Checks shared by every call that touches the pool.
+int check_pool(const gdr_step_args *a, const char *fn) {
+    if (!a) return fail(GDR_ERR_INVALID_ARG, "%s: args is NULL", fn);
+    if (a->batch < 0) return fail(GDR_ERR_INVALID_ARG, "%s: batch %d < 0", fn, a->batch);
+    if (a->nv <= 0 || a->nk <= 0)
+        return fail(GDR_ERR_INVALID_ARG, "%s: nv=%d, nk=%d must be positive", fn, a->nv, a->nk);
+    if (a->nv % a->nk != 0)
+        return fail(GDR_ERR_INVALID_ARG, "%s: nv=%d is not a multiple of nk=%d", fn, a->nv, a->nk);
+    if (a->K != a->V)
+        return fail(GDR_ERR_UNSUPPORTED, "%s: K=%d != V=%d (value head dim must equal key head dim)",
+                    fn, a->K, a->V);
+    if (!supported_dim(a->K))
+        return fail(GDR_ERR_UNSUPPORTED, "%s: K=%d not in {16,32,64,128}", fn, a->K);
+    if (a->state_dtype != GDR_F32 && a->state_dtype != GDR_BF16)
+        return fail(GDR_ERR_UNSUPPORTED, "%s: state_dtype %d", fn, a->state_dtype);
+    if (a->batch == 0) return GDR_OK;
+    if (!a->state || !a->slot_idx)
+        return fail(GDR_ERR_INVALID_ARG, "%s: state/slot_idx is NULL", fn);
+    if (a->max_slots <= 0) return fail(GDR_ERR_INVALID_ARG, "%s: max_slots %lld", fn, (long long)a->max_slots);
+    if (a->state_vdim_stride != 1)
+        return fail(GDR_ERR_UNSUPPORTED, "%s: state_vdim_stride must be 1 (got %lld)", fn,
+                    (long long)a->state_vdim_stride);
+    if (a->state_slot_stride <= 0 || a->state_head_stride <= 0 || a->state_kdim_stride <= 0)
+        return fail(GDR_ERR_INVALID_ARG, "%s: state strides must be positive", fn);
+    const long long es = esize(a->state_dtype);
+    if (!aligned16(a->state) || (a->state_slot_stride * es) % 16 || (a->state_head_stride * es) % 16 ||
+        (a->state_kdim_stride * es) % 16)
+        return fail(GDR_ERR_UNSUPPORTED, "%s: state base and strides must be 16-byte aligned", fn);
+    return GDR_OK;
+}
+
+// Checks for calls that read tokens and write output (fwd, verify, snapshots).
+int check_step(const gdr_step_args *a, const char *fn) {
+    int rc = check_pool(a, fn);
+    if (rc) return rc;
+    if (a->total_tokens < 0) return fail(GDR_ERR_INVALID_ARG, "%s: total_tokens < 0", fn);
+    if (a->total_tokens >= (1ll << 31))
+        return fail(GDR_ERR_UNSUPPORTED, "%s: total_tokens must be < 2^31", fn);
+    if (a->batch > 0 && !a->offsets) return fail(GDR_ERR_INVALID_ARG, "%s: offsets is NULL", fn);
+    if (a->total_tokens > 0) {
+        if (!a->qkv || !a->decay || !a->beta || !a->out)
+            return fail(GDR_ERR_INVALID_ARG, "%s: qkv/decay/beta/out is NULL", fn);
+        if (a->qkv_seq_stride <= 0 || a->qkv_chan_stride <= 0 || a->tok_seq_stride <= 0 ||
+            a->tok_head_stride <= 0 || a->out_seq_stride <= 0 || a->out_vdim_stride <= 0)
+            return fail(GDR_ERR_INVALID_ARG, "%s: token/output strides must be positive", fn);
+    }
+    if (!(a->eps >= 0.0f)) return fail(GDR_ERR_INVALID_ARG, "%s: eps must be >= 0", fn);
+    return GDR_OK;
+}
+
+gdr::StepParams lower(const gdr_step_args *a, unsigned *status) {
+    gdr::StepParams p{};
+    p.batch = a->batch;
+    p.nv = a->nv;
+    p.nk = a->nk;
+    p.r = a->nv / a->nk;
+    p.decay_is_log = a->decay_is_log ? 1 : 0;
+    p.l2norm = a->use_qk_l2norm ? 1 : 0;
+    p.T = a->total_tokens;
+    p.qkv = a->qkv;
+    p.qkv_ss = a->qkv_seq_stride;
+    p.qkv_cs = a->qkv_chan_stride;
+    p.decay = a->decay;
+    p.beta = a->beta;
+    p.tok_ss = a->tok_seq_stride;
+    p.tok_hs = a->tok_head_stride;
+    p.scale = a->scale > 0.0f ? a->scale : (float)(1.0 / std::sqrt((double)a->K));
+    p.eps = a->eps;
+    p.out = a->out;
+    p.out_ss = a->out_seq_stride;
+    p.out_vs = a->out_vdim_stride;
+    p.state = a->state;
+    p.st_slot = a->state_slot_stride;
+    p.st_head = a->state_head_stride;
+    p.st_k = a->state_kdim_stride;
+    p.max_slots = a->max_slots;
+    p.slot_idx = a->slot_idx;
+    p.offsets = a->offsets;
+    p.qkv_vec = (a->qkv_chan_stride == 1 && aligned16(a->qkv) && a->qkv_seq_stride % 4 == 0) ? 1 : 0;
+    p.out_vec = (a->out_vdim_stride == 1 && aligned16(a->out) && a->out_seq_stride % 4 == 0) ? 1 : 0;
+    p.status = status;
+    return p;
+}
+
+int launched(cudaError_t e, const char *fn) {
+    if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+    return ok();
+}
+
+int check_ring(int32_t ring_dtype, int64_t ring_rows, int32_t ring_len, int64_t record_stride,
+               const void *ring, const int32_t *ring_slot_idx, int K, int V, int r, int batch,
+               const char *fn) {
+    if (ring_dtype != GDR_F32)
+        return fail(GDR_ERR_UNSUPPORTED, "%s: ring_dtype must be GDR_F32", fn);
+    if (ring_len < 1 || ring_len > 32)
+        return fail(GDR_ERR_UNSUPPORTED, "%s: ring_len %d not in [1, 32]", fn, ring_len);
+    const int need = gdr_ring_record_elements(K, V, r);
+    if (record_stride < need || record_stride % 4)
+        return fail(GDR_ERR_INVALID_ARG, "%s: record_stride %lld must be a multiple of 4 and >= %d", fn,
+                    (long long)record_stride, need);
+    if (batch > 0 && (!ring || !ring_slot_idx || ring_rows <= 0))
+        return fail(GDR_ERR_INVALID_ARG, "%s: ring/ring_slot_idx NULL or ring_rows <= 0", fn);
+    return GDR_OK;
+}
+
+int check_inter(const gdr_step_args *a, const void *inter, int64_t s_slot, int64_t s_tok,
+                int64_t s_head, int32_t n_inter, const char *fn) {
+    if (a->batch == 0) return GDR_OK;
+    if (!inter) return fail(GDR_ERR_INVALID_ARG, "%s: intermediate buffer is NULL", fn);
+    if (n_inter < 1) return fail(GDR_ERR_INVALID_ARG, "%s: n_inter %d < 1", fn, n_inter);
+    if (s_slot <= 0 || s_tok <= 0 || s_head <= 0)
+        return fail(GDR_ERR_INVALID_ARG, "%s: intermediate strides must be positive", fn);
+    const long long es = esize(a->state_dtype);
+    if (!aligned16(inter) || (s_slot * es) % 16 || (s_tok * es) % 16 || (s_head * es) % 16)
+        return fail(GDR_ERR_UNSUPPORTED, "%s: intermediate base and strides must be 16-byte aligned", fn);
+    return GDR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdr_last_error(void) { return g_err.c_str(); }
+
+int gdr_version(void) { return 100; }
+
+int gdr_output_shape(int64_t total_tokens, int32_t nv, int32_t V, int64_t out_shape[2]) {
+    if (!out_shape || total_tokens < 0 || nv <= 0 || V <= 0)
+        return fail(GDR_ERR_INVALID_ARG, "gdr_output_shape: invalid arguments");
+    out_shape[0] = total_tokens;
+    out_shape[1] = (int64_t)nv * V;
+    return ok();
+}
+
+int gdr_ring_record_elements(int32_t K, int32_t V, int32_t ratio) {
+    if (K <= 0 || V <= 0 || ratio <= 0)
+        return fail(GDR_ERR_INVALID_ARG, "gdr_ring_record_elements: invalid arguments");
+    return K + ((ratio + 3) / 4) * 4 + ratio * V;
+}
+
+int gdr_fwd(const gdr_step_args *a, void *stream) {
+    int rc = check_step(a, "gdr_fwd");
+    if (rc) return rc;
+    if (a->batch == 0) return ok();
+    unsigned *st = nullptr;
+    if ((rc = status_ptr(&st))) return rc;
+    const gdr::StepParams p = lower(a, st);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (a->max_row_len == 1) return launched(gdr::launch_decode(p, a->K, a->state_dtype == GDR_BF16, s), "gdr_fwd");
+    return launched(gdr::launch_chain(p, a->K, a->state_dtype == GDR_BF16, gdr::Mode::Fwd, gdr::RingParams{},
+                                      gdr::SnapParams{}, a->max_row_len, s),
+                    "gdr_fwd");
+}
+
+int gdr_verify_ring(const gdr_step_args *a, float *ring, int32_t ring_dtype, int64_t ring_rows,
+                    int32_t ring_len, int64_t record_stride, const int32_t *ring_slot_idx, void *stream) {
+    int rc = check_step(a, "gdr_verify_ring");
+    if (rc) return rc;
+    const int r = a->nv / a->nk;
+    rc = check_ring(ring_dtype, ring_rows, ring_len, record_stride, ring, ring_slot_idx, a->K, a->V, r,
+                    a->batch, "gdr_verify_ring");
+    if (rc) return rc;
+    if (a->batch == 0) return ok();
+    unsigned *st = nullptr;
+    if ((rc = status_ptr(&st))) return rc;
+    const gdr::StepParams p = lower(a, st);
+    gdr::RingParams rp{};
+    rp.ring = ring;
+    rp.rows = ring_rows;
+    rp.len = ring_len;
+    rp.stride = record_stride;
+    rp.ring_slot = ring_slot_idx;
+    rp.alpha_off = a->K;
+    rp.u_off = a->K + ((r + 3) / 4) * 4;
+    return launched(gdr::launch_chain(p, a->K, a->state_dtype == GDR_BF16, gdr::Mode::Verify, rp,
+                                      gdr::SnapParams{}, a->max_row_len, static_cast<cudaStream_t>(stream)),
+                    "gdr_verify_ring");
+}
+
+int gdr_fold(const gdr_step_args *a, const float *ring, int32_t ring_dtype, int64_t ring_rows, int32_t ring_len,
+             int64_t record_stride, const int32_t *ring_slot_idx, const int32_t *counts, void *stream) {
+    int rc = check_pool(a, "gdr_fold");
+    if (rc) return rc;
+    const int r = a->nv / a->nk;
+    rc = check_ring(ring_dtype, ring_rows, ring_len, record_stride, ring, ring_slot_idx, a->K, a->V, r,
+                    a->batch, "gdr_fold");
+    if (rc) return rc;
+    if (a->batch == 0) return ok();
+    if (!counts) return fail(GDR_ERR_INVALID_ARG, "gdr_fold: counts is NULL");
+    unsigned *st = nullptr;
+    if ((rc = status_ptr(&st))) return rc;
+    gdr::FoldParams p{};
+    p.batch = a->batch;
+    p.nv = a->nv;
+    p.nk = a->nk;
+    p.r = r;
+    p.state = a->state;
+    p.st_slot = a->state_slot_stride;
+    p.st_head = a->state_head_stride;
+    p.st_k = a->state_kdim_stride;
+    p.max_slots = a->max_slots;
+    p.slot_idx = a->slot_idx;
+    p.ring = ring;
+    p.ring_rows = ring_rows;
+    p.ring_len = ring_len;
+    p.stride = record_stride;
+    p.ring_slot = ring_slot_idx;
+    p.counts = counts;
+    p.alpha_off = a->K;
+    p.u_off = a->K + ((r + 3) / 4) * 4;
+    p.status = st;
+    return launched(gdr::launch_fold(p, a->K, a->state_dtype == GDR_BF16, static_cast<cudaStream_t>(stream)),
+                    "gdr_fold");
+}
+
+int gdr_fwd_snapshots(const gdr_step_args *a, void *inter, int64_t inter_slot_stride, int64_t inter_token_stride,
+                      int64_t inter_head_stride, int32_t n_inter, int32_t steps_per_token, void *stream) {
+    int rc = check_step(a, "gdr_fwd_snapshots");
+    if (rc) return rc;
+    if (steps_per_token < 1) return fail(GDR_ERR_INVALID_ARG, "gdr_fwd_snapshots: steps_per_token < 1");
+    rc = check_inter(a, inter, inter_slot_stride, inter_token_stride, inter_head_stride, n_inter,
+                     "gdr_fwd_snapshots");
+    if (rc) return rc;
+    if (a->batch == 0) return ok();
+    unsigned *st = nullptr;
+    if ((rc = status_ptr(&st))) return rc;
+    const gdr::StepParams p = lower(a, st);
+    gdr::SnapParams sp{};
+    sp.inter = inter;
+    sp.s_slot = inter_slot_stride;
+    sp.s_tok = inter_token_stride;
+    sp.s_head = inter_head_stride;
+    sp.n_inter = n_inter;
+    sp.spt = steps_per_token;
+    return launched(gdr::launch_chain(p, a->K, a->state_dtype == GDR_BF16, gdr::Mode::Snap, gdr::RingParams{}, sp,
+                                      a->max_row_len, static_cast<cudaStream_t>(stream)),
+                    "gdr_fwd_snapshots");
+}
+
+int gdr_rollback(const gdr_step_args *a, const void *inter, int64_t inter_slot_stride, int64_t inter_token_stride,
+                 int64_t inter_head_stride, int32_t n_inter, const int32_t *accepted, void *stream) {
+    int rc = check_pool(a, "gdr_rollback");
+    if (rc) return rc;
+    rc = check_inter(a, inter, inter_slot_stride, inter_token_stride, inter_head_stride, n_inter, "gdr_rollback");
+    if (rc) return rc;
+    if (a->batch == 0) return ok();
+    if (!accepted) return fail(GDR_ERR_INVALID_ARG, "gdr_rollback: accepted is NULL");
+    unsigned *st = nullptr;
+    if ((rc = status_ptr(&st))) return rc;
+    gdr::RollbackParams p{};
+    p.batch = a->batch;
+    p.nv = a->nv;
+    p.state = a->state;
+    p.st_slot = a->state_slot_stride;
+    p.st_head = a->state_head_stride;
+    p.st_k = a->state_kdim_stride;
+    p.max_slots = a->max_slots;
+    p.slot_idx = a->slot_idx;
+    p.inter = inter;
+    p.s_slot = inter_slot_stride;
+    p.s_tok = inter_token_stride;
+    p.s_head = inter_head_stride;
+    p.n_inter = n_inter;
+    p.accepted = accepted;
+    p.status = st;
+    return launched(gdr::launch_rollback(p, a->K, a->state_dtype == GDR_BF16, static_cast<cudaStream_t>(stream)),
+                    "gdr_rollback");
+}
+
+int gdr_get_status(uint32_t *status, int32_t clear) {
+    if (!status) return fail(GDR_ERR_INVALID_ARG, "gdr_get_status: status is NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "gdr_get_status: %s", cudaGetErrorString(e));
+    unsigned v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_gdr_status, sizeof v);
+    if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "gdr_get_status: %s", cudaGetErrorString(e));
+    if (clear) {
+        const unsigned z = 0;
+        e = cudaMemcpyToSymbol(g_gdr_status, &z, sizeof z);
+        if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "gdr_get_status: %s", cudaGetErrorString(e));
+    }
+    *status = v;
+    return ok();
+}
+
+}  // extern "C"

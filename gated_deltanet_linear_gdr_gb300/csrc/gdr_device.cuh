@@ -1,0 +1,162 @@
+// Device-side building blocks shared by every GDR kernel.
+//
+// All kernels compute each token with ONE fixed sequence of float32 operations,
+// written here with explicit round-to-nearest intrinsics so the compiler cannot
+// contract or reorder them differently in different kernels:
+//
+//   * K-reductions (S^T k^, S^T q~, |q|^2, |k|^2, k.q) split the K rows into
+//     groups of 8 consecutive rows; a group's partial is a multiply followed by
+//     seven fused multiply-adds in ascending row order; group partials are
+//     combined by a pairwise tree whose first level adds groups (0,1),(2,3),...,
+//     the next ((0,1),(2,3)), and so on.  Any thread layout that gives a thread
+//     a run of consecutive groups and puts the remaining levels on lanes reached
+//     with xor-shuffles of increasing distance produces exactly this tree.
+//   * Per token, with S the state before the token's decay:
+//       a_j = sum_i S_ij k^_i,  b_j = sum_i S_ij q~_i   (q~ = q^ * scale)
+//       u_j = beta * (v_j - alpha * a_j)
+//       o_j = alpha * b_j + (k^ . q~) * u_j            (= scale * S_new^T q^)
+//       S_ij <- k^_i * u_j + alpha * S_ij
+//     which is the gated delta rule of "gated_delta_recurrence_fwd_gpu" and
+//     "core.ssm.ops.gdp.fused_recurrent" with the readout of the new state
+//     expanded, so one sweep over S serves both reductions.
+//
+// Because fwd, verify, fold and snapshots all apply the same advance
+// S <- fma(k^, u, alpha*S) with the same u, verify+fold over a prefix and the
+// forward pass over that prefix give identical bits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "gdr_internal.h"
+
+namespace gdr {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ void flag(unsigned *status, unsigned bit) {
+    if (status) atomicOr(status, bit);
+}
+
+// ---- storage types ---------------------------------------------------------
+// bfloat16 is carried as its raw 16-bit pattern (uint16_t).
+__device__ __forceinline__ float to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ float to_f32(float x) { return x; }
+
+template <typename ST> __device__ __forceinline__ ST from_f32(float x);
+template <> __device__ __forceinline__ uint16_t from_f32<uint16_t>(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+
+template <int BYTES> struct VecT;
+template <> struct VecT<16> { using T = uint4; };
+template <> struct VecT<8> { using T = uint2; };
+template <> struct VecT<4> { using T = uint32_t; };
+template <> struct VecT<2> { using T = uint16_t; };
+
+// C consecutive elements of storage type ST moved as one vector access.
+template <typename ST, int C> struct Pack {
+    static constexpr int BYTES = C * (int)sizeof(ST);
+    using VT = typename VecT<BYTES>::T;
+    union {
+        VT v;
+        ST e[C];
+    } u;
+    __device__ __forceinline__ float get(int i) const { return to_f32(u.e[i]); }
+    __device__ __forceinline__ void set(int i, float x) { u.e[i] = from_f32<ST>(x); }
+    __device__ __forceinline__ void load(const ST *p) { u.v = *reinterpret_cast<const VT *>(p); }
+    __device__ __forceinline__ void store(ST *p) const { *reinterpret_cast<VT *>(p) = u.v; }
+};
+
+// N floats from p[0], p[stride], ...; one vector load when allowed.
+template <int N>
+__device__ __forceinline__ void load_f32(const float *p, long long stride, bool vec, float (&x)[N]) {
+    if (vec) {
+        if constexpr (N % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < N; i += 4) {
+                float4 t = *reinterpret_cast<const float4 *>(p + i);
+                x[i] = t.x; x[i + 1] = t.y; x[i + 2] = t.z; x[i + 3] = t.w;
+            }
+            return;
+        } else if constexpr (N == 2) {
+            float2 t = *reinterpret_cast<const float2 *>(p);
+            x[0] = t.x; x[1] = t.y;
+            return;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = p[i * stride];
+}
+
+template <int N>
+__device__ __forceinline__ void store_f32(float *p, long long stride, bool vec, const float (&x)[N]) {
+    if (vec) {
+        if constexpr (N % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < N; i += 4)
+                *reinterpret_cast<float4 *>(p + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+            return;
+        } else if constexpr (N == 2) {
+            *reinterpret_cast<float2 *>(p) = make_float2(x[0], x[1]);
+            return;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) p[i * stride] = x[i];
+}
+
+// ---- the fixed per-token arithmetic ----------------------------------------
+
+__device__ __forceinline__ float chain_first(float x, float y) { return __fmul_rn(x, y); }
+__device__ __forceinline__ float chain_next(float x, float y, float p) { return __fmaf_rn(x, y, p); }
+
+// Pairwise tree over a thread's RG consecutive group partials (level 1 first).
+template <int N>
+__device__ __forceinline__ float tree(const float *p) {
+    if constexpr (N == 1) {
+        return p[0];
+    } else {
+        return __fadd_rn(tree<N / 2>(p), tree<N / 2>(p + N / 2));
+    }
+}
+
+// Remaining tree levels across the LK lanes that share a column (kl = lane % LK).
+template <int LK>
+__device__ __forceinline__ float tree_lanes(float x) {
+#pragma unroll
+    for (int m = 1; m < LK; m <<= 1) x = __fadd_rn(x, __shfl_xor_sync(kFull, x, m));
+    return x;
+}
+
+__device__ __forceinline__ float gdr_alpha(float g, int is_log) { return is_log ? expf(g) : g; }
+
+// From the reduced |q|^2, |k|^2 and raw k.q: the factors that turn raw q, k into
+// q~ = q * qs (scale folded in) and k^ = k * inv_k, and k^ . q~.
+__device__ __forceinline__ void gdr_norm_scalars(float ssq, float ssk, float kq_raw, int l2,
+                                                 float scale, float eps, float &inv_k, float &qs,
+                                                 float &kq) {
+    float inv_q = 1.0f;
+    inv_k = 1.0f;
+    if (l2) {
+        inv_q = rsqrtf(__fadd_rn(ssq, eps));
+        inv_k = rsqrtf(__fadd_rn(ssk, eps));
+    }
+    qs = __fmul_rn(inv_q, scale);
+    kq = __fmul_rn(kq_raw, __fmul_rn(inv_k, qs));
+}
+
+__device__ __forceinline__ float gdr_u(float beta, float alpha, float a, float v) {
+    return __fmul_rn(beta, __fmaf_rn(-alpha, a, v));
+}
+__device__ __forceinline__ float gdr_o(float alpha, float b, float kq, float u) {
+    return __fmaf_rn(alpha, b, __fmul_rn(kq, u));
+}
+__device__ __forceinline__ float gdr_advance(float s, float kh, float u, float alpha) {
+    return __fmaf_rn(kh, u, __fmul_rn(alpha, s));
+}
+
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
+}  // namespace gdr

@@ -1,0 +1,91 @@
+// Internal launch parameters shared by the host API (api.cu) and the kernels.
+// Host code validates gdr_step_args and lowers it into these plain structs,
+// which travel to the kernels by value.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdr.h"
+
+namespace gdr {
+
+// One recurrence call, after validation.  Strides in elements.
+struct StepParams {
+    int batch, nv, nk, r;  // r = nv / nk (GQA ratio)
+    int decay_is_log, l2norm;
+    long long T;
+    const float *qkv;
+    long long qkv_ss, qkv_cs;
+    const float *decay, *beta;
+    long long tok_ss, tok_hs;
+    float scale, eps;
+    float *out;
+    long long out_ss, out_vs;
+    void *state;
+    long long st_slot, st_head, st_k;  // value-dim stride is 1
+    long long max_slots;
+    const int *slot_idx, *offsets;
+    int qkv_vec;  // Q/K/V rows may be read with 16-byte vector loads
+    int out_vec;  // output rows may be written with 16-byte vector stores
+    unsigned *status;
+};
+
+// Verify ring ("gated_delta_recurrence_verify_ring_gpu", ring / ring_slot_idx).
+struct RingParams {
+    float *ring;
+    long long rows;
+    int len;
+    long long stride;  // elements per record
+    const int *ring_slot;
+    int alpha_off;     // = K
+    int u_off;         // = K + 4*ceil(r/4)
+};
+
+// Snapshots ("core.ssm.ops.gdp.fused_recurrent", intermediate_states).
+struct SnapParams {
+    void *inter;
+    long long s_slot, s_tok, s_head;
+    int n_inter;
+    int spt;
+};
+
+struct FoldParams {
+    int batch, nv, nk, r;
+    void *state;
+    long long st_slot, st_head, st_k;
+    long long max_slots;
+    const int *slot_idx;
+    const float *ring;
+    long long ring_rows;
+    int ring_len;
+    long long stride;
+    const int *ring_slot;
+    const int *counts;
+    int alpha_off, u_off;
+    unsigned *status;
+};
+
+struct RollbackParams {
+    int batch, nv;
+    void *state;
+    long long st_slot, st_head, st_k;
+    long long max_slots;
+    const int *slot_idx;
+    const void *inter;
+    long long s_slot, s_tok, s_head;
+    int n_inter;
+    const int *accepted;
+    unsigned *status;
+};
+
+enum class Mode : int { Fwd = 0, Verify = 1, Snap = 2 };
+
+// Launchers (defined next to their kernels).  Return cudaGetLastError().
+cudaError_t launch_decode(const StepParams &p, int K, bool bf16, cudaStream_t s);
+cudaError_t launch_chain(const StepParams &p, int K, bool bf16, Mode mode, const RingParams &rp,
+                         const SnapParams &sp, long long max_row_len, cudaStream_t s);
+cudaError_t launch_fold(const FoldParams &p, int K, bool bf16, cudaStream_t s);
+cudaError_t launch_rollback(const RollbackParams &p, int K, bool bf16, cudaStream_t s);
+
+}  // namespace gdr

@@ -1,0 +1,212 @@
+/*
+ * gdr.h -- C ABI of the GB300 gated delta rule (GDR) recurrence library (libgdr.so).
+ *
+ * The library runs the slot-indexed, ragged-batch gated delta rule recurrence
+ * and its speculative-decoding variants on one sm_103a GPU.  For every live
+ * sequence b and value head h, with key head hk = h / (nv / nk) and the
+ * state S = pool[slot_idx[b], h] stored [key index, value index], each token
+ * t of the row [offsets[b], offsets[b+1]) does
+ *
+ *     q^ = q / sqrt(|q|^2 + eps),  k^ = k / sqrt(|k|^2 + eps)   (use_qk_l2norm)
+ *     S  = alpha * S,   alpha = decay[t,h]  or  exp(decay[t,h])  (decay_is_log)
+ *     u  = beta[t,h] * (v - S^T k^)
+ *     S  = S + k^ u^T
+ *     out[t, h*V:(h+1)*V] = scale * S^T q^
+ *
+ * Sources: "gated_delta_recurrence_fwd_gpu" (Modular kernels API), summary and
+ * Args; "gated_delta_recurrence_verify_ring_gpu" (Modular Mojo API), summary
+ * and Args; "gated_delta_recurrence_fwd_shape" (Modular Mojo API);
+ * "core.ssm.ops.gdp.fused_recurrent" (Megatron-Core), module summary and the
+ * Parameters of fused_recurrent_gated_delta_rule_update.
+ *
+ * Conventions shared by every entry point
+ *   - Every buffer pointer is a DEVICE pointer owned by the caller; the library
+ *     allocates and frees nothing and keeps no pointer after a call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  They never synchronise and never read device memory on the host;
+ *     only gdr_get_status() synchronises.
+ *   - Strides are in ELEMENTS.  Arithmetic is float32; per-token inputs and the
+ *     output are float32; the pool is bfloat16 or float32.
+ *   - Return value: GDR_OK, or a negative code with a message available from
+ *     gdr_last_error() (thread-local).  Arguments are checked before anything
+ *     is launched; an error launches nothing.
+ *   - Problems the host cannot see (slot or ring row out of range, offsets not
+ *     monotone, a row longer than max_row_len, a bad count or accepted index)
+ *     are detected on the device: the affected (row, head) is skipped -- its
+ *     output rows are zeroed where the call writes output -- and a bit is set
+ *     in the device status word (GDR_STATUS_*), read with gdr_get_status().
+ *   - Results do not depend on how a batch is composed or on which kernel the
+ *     library picks: every pass uses one fixed order of float32 operations per
+ *     (row, head), so the same row gives the same bits in any call.
+ *   - Two live rows of one call must not share a pool slot (they would race).
+ */
+#ifndef GDR_H
+#define GDR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------- */
+#define GDR_OK 0
+#define GDR_ERR_INVALID_ARG (-1) /* null pointer, negative size, nv % nk != 0, bad stride */
+#define GDR_ERR_UNSUPPORTED (-2) /* K != V, K not in {16,32,64,128}, dtype, misalignment  */
+#define GDR_ERR_CUDA (-3)        /* a CUDA call or kernel launch failed                   */
+
+/* ---- device status bits (sticky until cleared by gdr_get_status) -------- */
+#define GDR_STATUS_BAD_SLOT 0x1u          /* slot_idx[b] < -1 or >= max_slots          */
+#define GDR_STATUS_BAD_OFFSETS 0x2u       /* offsets not monotone or beyond T          */
+#define GDR_STATUS_BAD_RING_SLOT 0x4u     /* ring_slot_idx[b] outside [0, ring_rows)   */
+#define GDR_STATUS_BAD_COUNT 0x8u         /* fold count < 0                            */
+#define GDR_STATUS_ROW_TOO_LONG 0x10u     /* a row longer than args.max_row_len        */
+#define GDR_STATUS_BAD_ACCEPTED 0x20u     /* rollback index outside [-1, n_inter)      */
+#define GDR_STATUS_SNAPSHOT_OVERFLOW 0x40u /* a row has more complete drafts than n_inter */
+
+/* ---- dtypes ------------------------------------------------------------- */
+typedef enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
+
+/*
+ * Arguments of one recurrence call ("gated_delta_recurrence_fwd_gpu", Args).
+ *
+ * qkv      [total_tokens, 2*nk*K + nv*V] float32, "qkv_conv_output": Q channels
+ *          [0, nk*K), K channels [nk*K, 2*nk*K), V channels [2*nk*K, 2*nk*K + nv*V);
+ *          key head hk occupies [hk*K, (hk+1)*K) inside its range, value head h
+ *          occupies [h*V, (h+1)*V).  Element (t, c) is at t*qkv_seq_stride +
+ *          c*qkv_chan_stride.
+ * decay    [total_tokens, nv] float32: alpha, or the log decay g when
+ *          decay_is_log != 0 ("core.ssm.ops.gdp.fused_recurrent", g).
+ * beta     [total_tokens, nv] float32.  decay and beta share tok_seq_stride /
+ *          tok_head_stride ("per_token_seqlen_stride", "per_token_head_stride").
+ * out      [total_tokens, nv*V] float32; element (t, j) at t*out_seq_stride +
+ *          j*out_vdim_stride.  Written for every token of every row.
+ * state    [max_slots, nv, K, V] pool of state_dtype, read and written in place at
+ *          slot_idx[b]; element (s, h, i, j) at s*state_slot_stride +
+ *          h*state_head_stride + i*state_kdim_stride + j*state_vdim_stride.
+ *          state_vdim_stride must be 1; the other three strides must keep every
+ *          8-element (bf16) / 4-element (f32) group 16-byte aligned, and so must
+ *          the base pointer.
+ * slot_idx [batch] int32: pool slot of each row, -1 = padding request (output
+ *          zeroed, nothing else written).  Same bits as the pages' uint32.
+ * offsets  [batch+1] int32: row b spans [offsets[b], offsets[b+1]).
+ * scale    query scale; <= 0 selects K^-0.5.
+ * eps      added to |q|^2 and |k|^2 under the square root (1e-6 is customary).
+ * max_row_len  an upper bound on every row's length, or <= 0 if unknown.  It only
+ *          selects the kernel (1 picks the single-token decode kernel); a row
+ *          longer than a positive bound is skipped and flagged
+ *          GDR_STATUS_ROW_TOO_LONG.
+ */
+typedef struct gdr_step_args {
+    int32_t batch;
+    int32_t nv;
+    int32_t nk;
+    int32_t K;
+    int32_t V;
+    int32_t decay_is_log;
+    int32_t use_qk_l2norm;
+    int32_t state_dtype; /* gdr_dtype */
+    int64_t total_tokens;
+    int64_t max_row_len;
+    const float *qkv;
+    int64_t qkv_seq_stride;
+    int64_t qkv_chan_stride;
+    const float *decay;
+    const float *beta;
+    int64_t tok_seq_stride;
+    int64_t tok_head_stride;
+    float scale;
+    float eps;
+    float *out;
+    int64_t out_seq_stride;
+    int64_t out_vdim_stride;
+    void *state;
+    int64_t state_slot_stride;
+    int64_t state_head_stride;
+    int64_t state_kdim_stride;
+    int64_t state_vdim_stride;
+    int64_t max_slots;
+    const int32_t *slot_idx;
+    const int32_t *offsets;
+} gdr_step_args;
+
+/* Message for the last error returned on this thread ("" if none). */
+const char *gdr_last_error(void);
+
+/* Library version, e.g. 100 for 0.1.0. */
+int gdr_version(void);
+
+/* Output shape of a recurrence call: out_shape = {total_tokens, nv*V}
+ * ("gated_delta_recurrence_fwd_shape": [total_seq_len, value_dim]). */
+int gdr_output_shape(int64_t total_tokens, int32_t nv, int32_t V, int64_t out_shape[2]);
+
+/* Minimum ring record length in elements for GQA ratio `ratio` = nv/nk
+ * ("gated_delta_recurrence_verify_ring_gpu", ring_record_stride: at least
+ * gated_delta_ring_record_elements(nv // nk)).  Record layout, float32:
+ *     [ k^ (K) | alpha_0 .. alpha_{ratio-1}, zero-padded to a multiple of 4 |
+ *       u_0 (V) | ... | u_{ratio-1} (V) ]
+ * where u_j and alpha_j belong to value head hk*ratio + j.  Returns the length
+ * (K + 4*ceil(ratio/4) + ratio*V) or a negative code. */
+int gdr_ring_record_elements(int32_t K, int32_t V, int32_t ratio);
+
+/* Forward pass ("gated_delta_recurrence_fwd_gpu"): runs every row over its
+ * tokens, writes out for every token and writes each live row's final state
+ * back to its slot (bf16 pools are rounded to nearest-even once, at the row
+ * end).  Rows of length 0 leave their slot untouched. */
+int gdr_fwd(const gdr_step_args *args, void *stream);
+
+/* Verify pass ("gated_delta_recurrence_verify_ring_gpu", summary): writes the
+ * same out as gdr_fwd and leaves the pool untouched, except that a row longer
+ * than ring_len records nothing and commits its state exactly as gdr_fwd does.
+ * A row with L <= ring_len writes record t - offsets[b] of
+ *     ring[ring_slot_idx[b], hk, :, :]   (ring is [ring_rows, nk, ring_len, record_stride])
+ * for each token, in the layout of gdr_ring_record_elements.  Padding rows
+ * write no records.  ring_dtype must be GDR_F32 (the fold is bit-exact against
+ * the forward pass only for float32 records); record_stride must be a multiple
+ * of 4 and at least gdr_ring_record_elements(K, V, nv/nk); 1 <= ring_len <= 32. */
+int gdr_verify_ring(const gdr_step_args *args, float *ring, int32_t ring_dtype,
+                    int64_t ring_rows, int32_t ring_len, int64_t record_stride,
+                    const int32_t *ring_slot_idx, void *stream);
+
+/* Fold ("gated_delta_recurrence_verify_ring_gpu", summary; the pages name the
+ * kernel gated_delta_state_fold_gpu): advances each live row's slot over the
+ * first counts[b] records of its ring row, S = alpha_t S + k^_t u_t^T, and
+ * writes it back.  counts[b] == 0 or counts[b] > ring_len leaves the row alone
+ * (a row longer than ring_len was already committed by the verify pass, so a
+ * caller passes its full length).  With a float32 ring the result equals
+ * gdr_fwd over the accepted prefix bit for bit.  Uses from `args`: batch, nv,
+ * nk, K, V, state*, max_slots, slot_idx (qkv/decay/beta/out/offsets unused). */
+int gdr_fold(const gdr_step_args *args, const float *ring, int32_t ring_dtype,
+             int64_t ring_rows, int32_t ring_len, int64_t record_stride,
+             const int32_t *ring_slot_idx, const int32_t *counts, void *stream);
+
+/* Forward pass with per-draft-token snapshots ("core.ssm.ops.gdp.fused_recurrent",
+ * intermediate_states and steps_per_token): as gdr_fwd, and in addition the
+ * state after step (i+1)*steps_per_token - 1 of a row is stored at
+ *     inter[slot, i, h, :, :]  = inter + slot*inter_slot_stride +
+ *                               i*inter_token_stride + h*inter_head_stride
+ * (a dense [K, V] block in the pool's dtype) for every i < n_inter.  A partial
+ * trailing draft is not stored; padding rows store nothing.  A row with more
+ * complete drafts than n_inter stores the first n_inter and sets
+ * GDR_STATUS_SNAPSHOT_OVERFLOW.  Strides must keep 16-byte alignment. */
+int gdr_fwd_snapshots(const gdr_step_args *args, void *inter, int64_t inter_slot_stride,
+                      int64_t inter_token_stride, int64_t inter_head_stride,
+                      int32_t n_inter, int32_t steps_per_token, void *stream);
+
+/* Rollback ("core.ssm.ops.gdp.fused_recurrent", intermediate_states: roll the
+ * recurrence back to any accepted prefix): state[slot_idx[b], h] <-
+ * inter[slot_idx[b], accepted[b], h] for every value head.  accepted[b] == -1
+ * or slot -1 skips the row.  Uses from `args`: batch, nv, K, V, state*,
+ * max_slots, slot_idx. */
+int gdr_rollback(const gdr_step_args *args, const void *inter, int64_t inter_slot_stride,
+                 int64_t inter_token_stride, int64_t inter_head_stride, int32_t n_inter,
+                 const int32_t *accepted, void *stream);
+
+/* Reads the current device's status word (GDR_STATUS_* bits) into *status and,
+ * if clear != 0, resets it.  Synchronises the device. */
+int gdr_get_status(uint32_t *status, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDR_H */

@@ -1,0 +1,181 @@
+"""Host-side checks of the C ABI: the library builds and loads, exports every
+symbol include/gdr.h declares (and nothing else), and rejects invalid
+arguments before touching CUDA.  No compute call is made here."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from gated_deltanet_linear_gdr_gb300 import _binding as B
+from gated_deltanet_linear_gdr_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdr.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = libbuild.build()
+    return B.load_library(path)
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdr_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["gdr_fwd", "gdr_verify_ring", "gdr_fold", "gdr_fwd_snapshots", "gdr_rollback",
+              "gdr_output_shape", "gdr_ring_record_elements", "gdr_last_error", "gdr_get_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_library_exports_nothing_else(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    syms = {s for s in syms if not s.startswith("_") or s.startswith("gdr")}
+    assert syms == set(declared_functions()), syms ^ set(declared_functions())
+
+
+def test_struct_layout_matches_header():
+    # int32 x 8, int64 x 2, then pointers/int64s; 200 bytes on LP64
+    assert ctypes.sizeof(B.gdr_step_args) == 200
+    assert B.gdr_step_args.total_tokens.offset == 32
+    assert B.gdr_step_args.qkv.offset == 48
+    assert B.gdr_step_args.scale.offset == 104
+    assert B.gdr_step_args.state.offset == 136
+    assert B.gdr_step_args.offsets.offset == 192
+
+
+def test_helpers(lib):
+    assert lib.gdr_version() == 100
+    shp = (ctypes.c_int64 * 2)()
+    assert lib.gdr_output_shape(647, 32, 128, shp) == 0
+    assert (shp[0], shp[1]) == (647, 4096)
+    assert lib.gdr_output_shape(-1, 32, 128, shp) == B.GDR_ERR_INVALID_ARG
+    assert lib.gdr_ring_record_elements(128, 128, 2) == 388
+    assert lib.gdr_ring_record_elements(16, 16, 1) == 36
+    assert lib.gdr_ring_record_elements(64, 64, 5) == 64 + 8 + 320
+    assert lib.gdr_ring_record_elements(0, 16, 1) == B.GDR_ERR_INVALID_ARG
+
+
+def _valid_args():
+    a = B.gdr_step_args()
+    a.batch, a.nv, a.nk, a.K, a.V = 2, 4, 2, 16, 16
+    a.state_dtype = B.GDR_BF16
+    a.total_tokens = 8
+    fake = 0x7f0000000000  # never dereferenced: every case below fails validation first
+    a.qkv, a.qkv_seq_stride, a.qkv_chan_stride = fake, 2 * 2 * 16 + 4 * 16, 1
+    a.decay, a.beta, a.tok_seq_stride, a.tok_head_stride = fake, fake, 4, 1
+    a.out, a.out_seq_stride, a.out_vdim_stride = fake, 64, 1
+    a.state = fake
+    a.state_slot_stride, a.state_head_stride, a.state_kdim_stride, a.state_vdim_stride = (
+        4 * 256, 256, 16, 1)
+    a.max_slots = 4
+    a.slot_idx = a.offsets = fake
+    a.eps = 1e-6
+    return a
+
+
+BAD = [
+    ("K != V", lambda a: setattr(a, "V", 32), B.GDR_ERR_UNSUPPORTED),
+    ("K unsupported", lambda a: (setattr(a, "K", 48), setattr(a, "V", 48)), B.GDR_ERR_UNSUPPORTED),
+    ("nv % nk", lambda a: setattr(a, "nk", 3), B.GDR_ERR_INVALID_ARG),
+    ("nv <= 0", lambda a: setattr(a, "nv", 0), B.GDR_ERR_INVALID_ARG),
+    ("batch < 0", lambda a: setattr(a, "batch", -1), B.GDR_ERR_INVALID_ARG),
+    ("dtype", lambda a: setattr(a, "state_dtype", 7), B.GDR_ERR_UNSUPPORTED),
+    ("vdim stride", lambda a: setattr(a, "state_vdim_stride", 2), B.GDR_ERR_UNSUPPORTED),
+    ("misaligned state", lambda a: setattr(a, "state", 0x7f0000000002), B.GDR_ERR_UNSUPPORTED),
+    ("misaligned kdim stride", lambda a: setattr(a, "state_kdim_stride", 17), B.GDR_ERR_UNSUPPORTED),
+    ("null state", lambda a: setattr(a, "state", None), B.GDR_ERR_INVALID_ARG),
+    ("null slot_idx", lambda a: setattr(a, "slot_idx", None), B.GDR_ERR_INVALID_ARG),
+    ("null qkv", lambda a: setattr(a, "qkv", None), B.GDR_ERR_INVALID_ARG),
+    ("null out", lambda a: setattr(a, "out", None), B.GDR_ERR_INVALID_ARG),
+    ("null offsets", lambda a: setattr(a, "offsets", None), B.GDR_ERR_INVALID_ARG),
+    ("max_slots", lambda a: setattr(a, "max_slots", 0), B.GDR_ERR_INVALID_ARG),
+    ("T < 0", lambda a: setattr(a, "total_tokens", -5), B.GDR_ERR_INVALID_ARG),
+    ("zero stride", lambda a: setattr(a, "qkv_seq_stride", 0), B.GDR_ERR_INVALID_ARG),
+    ("eps < 0", lambda a: setattr(a, "eps", -1.0), B.GDR_ERR_INVALID_ARG),
+]
+
+
+@pytest.mark.parametrize("name,mutate,code", BAD, ids=[b[0] for b in BAD])
+def test_fwd_rejects_invalid_arguments(lib, name, mutate, code):
+    a = _valid_args()
+    mutate(a)
+    assert lib.gdr_fwd(ctypes.byref(a), None) == code
+    assert lib.gdr_last_error().decode()  # a message is set
+    assert lib.gdr_fwd(None, None) == B.GDR_ERR_INVALID_ARG
+
+
+def test_verify_and_fold_reject_bad_ring(lib):
+    a = _valid_args()
+    a.V = a.K = 16
+    a.state = 0x7f0000000002  # still invalid: proves the ring is checked only after args...
+    a.state = 0x7f0000000000
+    fake = 0x7f0000000000
+    need = lib.gdr_ring_record_elements(16, 16, 2)
+    a.state_dtype = B.GDR_F32
+    # bad ring dtype, length, stride, null pointers
+    assert lib.gdr_verify_ring(ctypes.byref(a), fake, B.GDR_BF16, 4, 8, need, fake, None) == \
+        B.GDR_ERR_UNSUPPORTED
+    assert lib.gdr_verify_ring(ctypes.byref(a), fake, B.GDR_F32, 4, 0, need, fake, None) == \
+        B.GDR_ERR_UNSUPPORTED
+    assert lib.gdr_verify_ring(ctypes.byref(a), fake, B.GDR_F32, 4, 33, need, fake, None) == \
+        B.GDR_ERR_UNSUPPORTED
+    assert lib.gdr_verify_ring(ctypes.byref(a), fake, B.GDR_F32, 4, 8, need - 4, fake, None) == \
+        B.GDR_ERR_INVALID_ARG
+    assert lib.gdr_verify_ring(ctypes.byref(a), fake, B.GDR_F32, 4, 8, need + 2, fake, None) == \
+        B.GDR_ERR_INVALID_ARG
+    assert lib.gdr_verify_ring(ctypes.byref(a), None, B.GDR_F32, 4, 8, need, fake, None) == \
+        B.GDR_ERR_INVALID_ARG
+    assert lib.gdr_fold(ctypes.byref(a), fake, B.GDR_F32, 4, 8, need, fake, None, None) == \
+        B.GDR_ERR_INVALID_ARG  # counts NULL
+    assert lib.gdr_fold(ctypes.byref(a), fake, B.GDR_F32, 0, 8, need, fake, fake, None) == \
+        B.GDR_ERR_INVALID_ARG  # ring_rows 0
+
+
+def test_snapshots_and_rollback_reject_bad_buffers(lib):
+    a = _valid_args()
+    fake = 0x7f0000000000
+    a.state_dtype = B.GDR_F32
+    hs = 16 * 16
+    assert lib.gdr_fwd_snapshots(ctypes.byref(a), fake, 4 * 4 * hs, 4 * hs, hs, 4, 0, None) == \
+        B.GDR_ERR_INVALID_ARG  # steps_per_token 0
+    assert lib.gdr_fwd_snapshots(ctypes.byref(a), None, 4 * 4 * hs, 4 * hs, hs, 4, 2, None) == \
+        B.GDR_ERR_INVALID_ARG
+    assert lib.gdr_fwd_snapshots(ctypes.byref(a), fake, 4 * 4 * hs, 4 * hs, hs, 0, 2, None) == \
+        B.GDR_ERR_INVALID_ARG
+    assert lib.gdr_fwd_snapshots(ctypes.byref(a), fake + 4, 4 * 4 * hs, 4 * hs, hs, 4, 2, None) == \
+        B.GDR_ERR_UNSUPPORTED
+    assert lib.gdr_rollback(ctypes.byref(a), fake, 4 * 4 * hs, 4 * hs, hs, 4, None, None) == \
+        B.GDR_ERR_INVALID_ARG
+    assert lib.gdr_rollback(ctypes.byref(a), fake, 4 * 4 * hs, 4 * hs + 1, hs, 4, fake, None) == \
+        B.GDR_ERR_UNSUPPORTED
+
+
+def test_empty_batch_is_a_no_op(lib):
+    a = _valid_args()
+    a.batch = 0
+    assert lib.gdr_fwd(ctypes.byref(a), None) == B.GDR_OK
+
+
+def test_status_null_pointer(lib):
+    assert lib.gdr_get_status(None, 0) == B.GDR_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="no CPU or Python fallback"):
+        B.load_library(str(tmp_path / "libgdr.so"))

@@ -1,0 +1,247 @@
+"""Contracts the pages state exactly, checked GPU against GPU, bit for bit:
+verify writes the forward pass's output and leaves the pool alone; verify +
+fold over a prefix equals the forward pass over it (float32 ring); long rows
+commit like the forward pass; snapshots and rollback equal the forward pass
+over the draft prefix; and the library's own guarantees (kernel choice,
+batch composition, strides and repeated runs do not change any bit)."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_gdr_gb300 as gdr
+from gated_deltanet_linear_gdr_gb300 import workloads as W
+from tests.gpu_helpers import DEV, Dev, pool_to_dev, pool_to_host, ring_for
+from tests.helpers import sub_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    gdr.gdr_get_status(clear=True)
+    yield
+
+
+def _prefix(w, b, n):
+    """Row b of w cut to its first n tokens, as a one-row workload."""
+    sub = sub_workload(w, [b])
+    return dataclasses.replace(sub, offsets=np.array([0, n], np.int32), qkv=sub.qkv[:n],
+                               decay=sub.decay[:n], beta=sub.beta[:n])
+
+
+def _run_fwd(w, pool, max_row_len=0):
+    d = Dev(w, pool)
+    out = d.fwd(max_row_len=max_row_len)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), pool_to_host(d.state)
+
+
+@pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
+def test_verify_output_equals_forward_and_pool_untouched(state_dtype):
+    w = W.verify_fold(batch=24, max_slots=48, ring_rows=48, state_dtype=state_dtype)
+    pool = w.state_pool()
+    out_f, pool_f = _run_fwd(w, pool)
+    d = Dev(w, pool)
+    ring = ring_for(w, w.ring_len, w.ring_rows)
+    out_v = d.verify(ring, torch.from_numpy(w.ring_slot_idx).to(DEV)).cpu().numpy()
+    assert (out_v.view(np.uint32) == out_f.view(np.uint32)).all()
+    host = pool_to_host(d.state)
+    for b in range(w.batch):
+        s = int(w.slot_idx[b])
+        if w.row_lengths[b] > w.ring_len:
+            assert (host[s] == pool_f[s]).all(), "long row must commit exactly like fwd"
+            assert torch.isnan(ring[int(w.ring_slot_idx[b])]).all(), "long row must not record"
+        else:
+            assert (host[s] == pool[s]).all(), "verify must leave the pool alone"
+
+
+@pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
+def test_verify_plus_fold_equals_forward_over_prefix(state_dtype):
+    w = W.verify_fold(batch=24, max_slots=48, ring_rows=48, state_dtype=state_dtype)
+    counts = np.array([b % 6 for b in range(w.batch)], np.int32)
+    counts[-1] = w.row_lengths[-1]
+    w = dataclasses.replace(w, counts=counts)
+    pool = w.state_pool()
+    d = Dev(w, pool)
+    ring = ring_for(w, w.ring_len, w.ring_rows)
+    rsi = torch.from_numpy(w.ring_slot_idx).to(DEV)
+    d.verify(ring, rsi)
+    gdr.gdr_fold(d.state, d.slot, ring, rsi, torch.from_numpy(counts).to(DEV))
+    torch.cuda.synchronize()
+    host = pool_to_host(d.state)
+    _, pool_full = _run_fwd(w, pool)
+    for b in range(w.batch):
+        s = int(w.slot_idx[b])
+        c = int(counts[b])
+        if w.row_lengths[b] > w.ring_len:
+            assert (host[s] == pool_full[s]).all()
+            continue
+        if c == 0:
+            assert (host[s] == pool[s]).all()
+            continue
+        _, pool_pref = _run_fwd(_prefix(w, b, c), pool)
+        assert (host[s] == pool_pref[s]).all(), f"row {b} count {c}"
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_snapshots_and_rollback_equal_forward_over_prefix(state_dtype):
+    w = W.gdp_snapshots(batch=6, max_slots=12, state_dtype=state_dtype)
+    pool = w.state_pool()
+    d = Dev(w, pool)
+    tdt = torch.bfloat16 if state_dtype == "bf16" else torch.float32
+    inter = torch.zeros((w.max_slots, w.n_inter, w.nv, w.K, w.V), dtype=tdt, device=DEV)
+    out_s = d.snapshots(inter, w.steps_per_token).cpu().numpy()
+    host_inter = pool_to_host(inter)
+    final = pool_to_host(d.state)
+    out_f, pool_f = _run_fwd(w, pool)
+    assert (out_s.view(np.uint32) == out_f.view(np.uint32)).all()
+    assert (final == pool_f).all()
+    M = w.steps_per_token
+    for b in range(w.batch):
+        s = int(w.slot_idx[b])
+        for i in range(w.n_inter):
+            _, pp = _run_fwd(_prefix(w, b, (i + 1) * M), pool)
+            assert (host_inter[s, i] == pp[s]).all(), (b, i)
+        assert (host_inter[s, w.n_inter - 1] == final[s]).all()
+    acc = torch.from_numpy(w.accepted).to(DEV)
+    gdr.gdr_rollback(d.state, d.slot, inter, acc)
+    host = pool_to_host(d.state)
+    for b in range(w.batch):
+        s = int(w.slot_idx[b])
+        _, pp = _run_fwd(_prefix(w, b, (int(w.accepted[b]) + 1) * M), pool)
+        assert (host[s] == pp[s]).all()
+
+
+def test_chaining_float32_pool():
+    """float32 pool: one call over L tokens == two calls over L1 and L - L1."""
+    w = W.random_case(600, [23, 40], nk=2, nv=4, K=128, max_slots=4, state_dtype="f32")
+    pool = w.state_pool()
+    out, full = _run_fwd(w, pool)
+    st = pool.copy()
+    cuts = [10, 17]
+    parts = []
+    for first in (True, False):
+        rows = []
+        for b in range(w.batch):
+            t0, t1 = int(w.offsets[b]), int(w.offsets[b + 1])
+            c = t0 + cuts[b]
+            rows.append((t0, c) if first else (c, t1))
+        toks = np.concatenate([np.arange(a, z) for a, z in rows])
+        offs = np.concatenate([[0], np.cumsum([z - a for a, z in rows])]).astype(np.int32)
+        part = dataclasses.replace(w, qkv=w.qkv[toks], decay=w.decay[toks], beta=w.beta[toks],
+                                   offsets=offs)
+        o, st = _run_fwd(part, st)
+        parts.append((o, rows))
+    assert (st == full).all()
+
+
+def test_decode_kernel_equals_general_kernel():
+    w = W.decode(batch=48, max_slots=96)
+    pool = w.state_pool()
+    o1, s1 = _run_fwd(w, pool, max_row_len=1)
+    o2, s2 = _run_fwd(w, pool, max_row_len=0)
+    assert (o1.view(np.uint32) == o2.view(np.uint32)).all()
+    assert (s1 == s2).all()
+
+
+def test_batch_composition_does_not_change_bits():
+    w = W.random_case(601, [5, 31, 1, 12], nk=2, nv=4, K=64, max_slots=6, state_dtype="bf16")
+    pool = w.state_pool()
+    out, st = _run_fwd(w, pool)
+    for b in range(w.batch):
+        o, s = _run_fwd(sub_workload(w, [b]), pool)
+        t0, t1 = int(w.offsets[b]), int(w.offsets[b + 1])
+        assert (o.view(np.uint32) == out[t0:t1].view(np.uint32)).all()
+        assert (s[w.slot_idx[b]] == st[w.slot_idx[b]]).all()
+
+
+def test_repeated_runs_are_identical():
+    w = W.random_case(602, [17, 9], nk=2, nv=4, K=128, max_slots=4, state_dtype="bf16")
+    pool = w.state_pool()
+    a = _run_fwd(w, pool)
+    b = _run_fwd(w, pool)
+    assert (a[0].view(np.uint32) == b[0].view(np.uint32)).all() and (a[1] == b[1]).all()
+
+
+def test_strided_views_equal_contiguous():
+    """qkv, decay/beta and out as views with padded strides; a pool with padded
+    rows -- same bits as the dense call."""
+    w = W.random_case(603, [6, 19], nk=2, nv=4, K=64, max_slots=4, state_dtype="bf16")
+    pool = w.state_pool()
+    out_ref, st_ref = _run_fwd(w, pool)
+    T, C = w.qkv.shape
+    big = torch.zeros((T, C + 36), device=DEV)
+    big[:, 4:4 + C] = torch.from_numpy(w.qkv).to(DEV)
+    qkv = big[:, 4:4 + C]
+    db = torch.zeros((T, 2 * w.nv + 8), device=DEV)
+    db[:, :w.nv] = torch.from_numpy(w.decay).to(DEV)
+    decay = db[:, :w.nv]
+    bb = torch.zeros((T, 2 * w.nv + 8), device=DEV)
+    bb[:, 3:3 + w.nv] = torch.from_numpy(w.beta).to(DEV)
+    beta = bb[:, 3:3 + w.nv]
+    ob = torch.zeros((T, w.nv * w.V * 2), device=DEV)
+    out = ob[:, ::2]  # value-dim stride 2 (scalar stores)
+    sbig = torch.zeros((w.max_slots, w.nv, w.K, w.V + 8), dtype=torch.bfloat16, device=DEV)
+    sbig[..., :w.V] = pool_to_dev(pool)
+    state = sbig[..., :w.V]
+    gdr.gdr_fwd(qkv, decay, beta, state, torch.from_numpy(w.slot_idx).to(DEV),
+                torch.from_numpy(w.offsets).to(DEV), out=out)
+    torch.cuda.synchronize()
+    assert (out.cpu().numpy().view(np.uint32) == out_ref.view(np.uint32)).all()
+    assert (pool_to_host(state.contiguous()) == st_ref).all()
+
+
+def test_beta0_decay1_leaves_bf16_state_bitwise():
+    w = W.random_case(604, [7, 1], nk=1, nv=2, K=128, max_slots=3, state_dtype="bf16")
+    w = dataclasses.replace(w, decay=np.ones_like(w.decay), beta=np.zeros_like(w.beta))
+    pool = w.state_pool()
+    _, st = _run_fwd(w, pool)
+    assert (st == pool).all()
+    _, st = _run_fwd(dataclasses.replace(w, offsets=np.array([0, 1, 2], np.int32),
+                                         qkv=w.qkv[:2], decay=w.decay[:2], beta=w.beta[:2]),
+                     pool, max_row_len=1)
+    assert (st == pool).all()
+
+
+def test_padding_rows_write_nothing_but_zero_output():
+    w = W.random_case(605, [4, 3, 2], nk=2, nv=4, K=32, max_slots=5, state_dtype="f32")
+    w = dataclasses.replace(w, slot_idx=np.array([1, -1, 3], np.int32))
+    pool = w.state_pool()
+    d = Dev(w, pool)
+    out = torch.full((w.total_tokens, w.nv * w.V), float("nan"), device=DEV)
+    d.fwd(out=out)
+    ring = ring_for(w, 8, 5)
+    d2 = Dev(w, pool)
+    out2 = d2.verify(ring, torch.tensor([0, 1, 2], dtype=torch.int32, device=DEV))
+    inter = torch.full((5, 2, w.nv, w.K, w.V), float("nan"), device=DEV)
+    d3 = Dev(w, pool)
+    out3 = d3.snapshots(inter, 1)
+    torch.cuda.synchronize()
+    for o in (out, out2, out3):
+        assert (o[4:7] == 0).all()
+    for dd in (d, d2, d3):
+        assert (pool_to_host(dd.state)[[0, 2, 4]] == pool[[0, 2, 4]]).all()
+    assert torch.isnan(ring[1]).all()
+    assert torch.isnan(inter[[0, 2, 4]]).all()
+
+
+def test_device_status_flags_bad_inputs():
+    w = W.random_case(606, [2, 1, 3], nk=1, nv=2, K=16, max_slots=4, state_dtype="f32")
+    pool = w.state_pool()
+    bad = dataclasses.replace(w, slot_idx=np.array([0, 9, 2], np.int32))
+    d = Dev(bad, pool)
+    out = torch.full((w.total_tokens, w.nv * w.V), float("nan"), device=DEV)
+    d.fwd(out=out)
+    st = gdr.gdr_get_status(clear=True)
+    assert st & 0x1, gdr.status_names(st)
+    assert (out[2:3] == 0).all()                     # the bad row's output is zeroed
+    assert (pool_to_host(d.state)[[1, 3]] == pool[[1, 3]]).all()
+    d = Dev(w, pool)
+    d.fwd(max_row_len=2)                              # a row of 3 tokens breaks the bound
+    st = gdr.gdr_get_status(clear=True)
+    assert st & 0x10, gdr.status_names(st)
+    assert gdr.gdr_get_status(clear=True) == 0

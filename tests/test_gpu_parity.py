@@ -1,0 +1,228 @@
+"""GPU path vs the CPU oracle on the same seeded inputs, through the C ABI.
+
+Tolerances: outputs max abs 2e-3; bf16 state within one bf16 ulp of the
+oracle (floor 2^-10); float32 state, ring and snapshots 1e-4 abs/rel; slot,
+record and snapshot bookkeeping exact."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gated_deltanet_linear_gdr_gb300 as gdr
+from gated_deltanet_linear_gdr_gb300 import workloads as W
+from tests.gpu_helpers import (DEV, Dev, check_out, check_state, pool_to_dev, pool_to_host,
+                               ring_for)
+from tests.helpers import problem, sub_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    gdr.gdr_get_status(clear=True)
+    yield
+    st = gdr.gdr_get_status(clear=True)
+    assert st == 0, f"device status {gdr.status_names(st)}"
+
+
+def _fwd_parity(w, max_row_len=0):
+    pool = w.state_pool()
+    d = Dev(w, pool)
+    out = d.fwd(max_row_len=max_row_len)
+    torch.cuda.synchronize()
+    p = problem(w, state=pool.copy())
+    ref = oracle.fwd(p)
+    check_out(out, ref)
+    check_state(pool_to_host(d.state), p.state)
+    return out, d, p
+
+
+def test_tiny_config():
+    _fwd_parity(W.tiny())
+
+
+@pytest.mark.parametrize("K", [16, 32, 64, 128])
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_ragged_rows_all_head_dims(K, state_dtype):
+    # lengths span several staged chunks (16 tokens) with ragged tails, plus empty
+    # and single-token rows and a padding row; GQA ratio 2
+    lengths = [37, 0, 1, 16, 5, 33]
+    w = W.random_case(100 + K, lengths, nk=2, nv=4, K=K, max_slots=9, state_dtype=state_dtype,
+                      n_pad=1)
+    _fwd_parity(w)
+
+
+@pytest.mark.parametrize("K", [16, 32, 64, 128])
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_decode_kernel_all_head_dims(K, state_dtype):
+    w = W.random_case(200 + K, [1] * 7 + [0], nk=2, nv=6, K=K, max_slots=12,
+                      state_dtype=state_dtype, n_pad=2)
+    _fwd_parity(w, max_row_len=1)
+
+
+@pytest.mark.parametrize("variant", ["no_l2norm", "log_decay", "scale", "gqa4", "mha"])
+def test_variants(variant):
+    kw = dict(nk=2, nv=4, K=64, max_slots=6, state_dtype="bf16")
+    if variant == "no_l2norm":
+        w = W.random_case(300, [9, 20], use_l2norm=False, state_std=0.02, **kw)
+        # raw q/k are unnormalised: keep the output scale comparable to the tolerance
+        w = dataclasses.replace(w, qkv=w.qkv * np.float32(0.125))
+    elif variant == "log_decay":
+        w = W.random_case(301, [9, 20], decay_is_log=True, **kw)
+    elif variant == "scale":
+        w = W.random_case(302, [9, 20], scale=0.3, **kw)
+    elif variant == "gqa4":
+        w = W.random_case(303, [9, 20], **{**kw, "nk": 1})
+    else:
+        w = W.random_case(304, [9, 20], **{**kw, "nk": 4})
+    _fwd_parity(w)
+    _fwd_parity(dataclasses.replace(w, offsets=w.offsets), max_row_len=0)
+
+
+def test_decode_config_full_size():
+    """The decode workload exactly as timed: batch 256, one token, 8 padding rows,
+    nk=16, nv=32, K=V=128, bf16 pool [512, 32, 128, 128]."""
+    w = W.decode()
+    out, d, p = _fwd_parity(w, max_row_len=1)
+    pad = w.slot_idx < 0
+    assert (out.cpu().numpy()[pad] == 0).all()
+
+
+def test_decode_config_through_general_kernel():
+    w = W.decode(batch=64, max_slots=128)
+    _fwd_parity(w, max_row_len=0)
+
+
+def test_prefill_config_sampled_rows():
+    """The ragged prefill workload at full size on the GPU; the oracle recomputes
+    the two shortest rows (rows are independent)."""
+    w = W.prefill()
+    pool = w.state_pool()
+    d = Dev(w, pool)
+    out = d.fwd()
+    torch.cuda.synchronize()
+    L = w.row_lengths
+    rows = list(np.argsort(L)[:2])
+    sub = sub_workload(w, rows)
+    p = problem(sub, state=pool.copy())
+    ref = oracle.fwd(p)
+    got = out.cpu().numpy()
+    toks = np.concatenate([np.arange(w.offsets[b], w.offsets[b + 1]) for b in rows])
+    err = np.abs(got[toks].astype(np.float64) - ref).max()
+    assert err <= 2e-3, err
+    host = pool_to_host(d.state)
+    check_state(host, p.state, slots=[int(w.slot_idx[b]) for b in rows])
+
+
+def test_verify_fold_config():
+    w = W.verify_fold()
+    pool = w.state_pool()
+    d = Dev(w, pool)
+    ring = ring_for(w, w.ring_len, w.ring_rows)
+    rsi = torch.from_numpy(w.ring_slot_idx).to(DEV)
+    out = d.verify(ring, rsi)
+    torch.cuda.synchronize()
+    pv = problem(w, state=pool.copy())
+    oring = np.full(tuple(ring.shape), np.nan, np.float32)
+    ref = oracle.verify_ring(pv, oring, w.ring_slot_idx, w.ring_len)
+    check_out(out, ref)
+    host = pool_to_host(d.state)
+    long_rows = [b for b in range(w.batch) if w.row_lengths[b] > w.ring_len]
+    for b in range(w.batch):
+        s = int(w.slot_idx[b])
+        if b in long_rows:
+            check_state(host, pv.state, slots=[s])
+        else:
+            assert (host[s] == pool[s]).all(), "verify wrote the pool"
+    # records: same fields written, values within float32 tolerance
+    g = ring.cpu().numpy()
+    assert (np.isnan(g) == np.isnan(oring)).all()
+    m = ~np.isnan(oring)
+    np.testing.assert_allclose(g[m], oring[m], rtol=1e-4, atol=1e-4)
+    # fold with the accepted counts, against the oracle's fold of its own records
+    cnt = torch.from_numpy(w.counts).to(DEV)
+    gdr.gdr_fold(d.state, d.slot, ring, rsi, cnt)
+    torch.cuda.synchronize()
+    oracle.fold(pv, oring, w.ring_slot_idx, w.counts, w.ring_len)
+    check_state(pool_to_host(d.state), pv.state, slots=w.live_slots())
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_fold_on_synthetic_ring(state_dtype):
+    """Fold alone on a random ring (not produced by any verify pass)."""
+    nk, nv, K, ring_len = 2, 4, 128, 8
+    w = W.random_case(400, [1] * 6, nk=nk, nv=nv, K=K, max_slots=10, state_dtype=state_dtype)
+    w = dataclasses.replace(w, slot_idx=np.array([3, -1, 7, 0, 9, 5], np.int32))
+    stride = gdr.gdr_ring_record_elements(K, K, nv // nk)
+    rng = np.random.default_rng(401)
+    ring = (rng.standard_normal((6, nk, ring_len, stride)) * 0.3).astype(np.float32)
+    ring[..., K:K + 4] = rng.uniform(0.8, 1.0, (6, nk, ring_len, 4)).astype(np.float32)
+    rsi = np.array([5, 4, 3, 2, 1, 0], np.int32)
+    counts = np.array([3, 2, 0, 8, 9, 1], np.int32)
+    pool = w.state_pool()
+    st = pool_to_dev(pool)
+    gdr.gdr_fold(st, torch.from_numpy(w.slot_idx).to(DEV), torch.from_numpy(ring).to(DEV),
+                 torch.from_numpy(rsi).to(DEV), torch.from_numpy(counts).to(DEV))
+    torch.cuda.synchronize()
+    p = problem(w, state=pool.copy())
+    oracle.fold(p, ring, rsi, counts, ring_len)
+    host = pool_to_host(st)
+    check_state(host, p.state)
+    for b, s in enumerate(w.slot_idx):
+        if s >= 0 and (counts[b] == 0 or counts[b] > ring_len):
+            assert (host[s] == pool[s]).all()
+
+
+def test_gdp_snapshot_config_and_rollback():
+    """Gated Delta Product spec-decode at full size: 64 requests x 4 drafts x 2
+    Householder copies, fp32 cache [128, 32, 128, 128], snapshots every 2 steps,
+    then rollback to a random accepted draft."""
+    w = W.gdp_snapshots()
+    pool = w.state_pool()
+    d = Dev(w, pool)
+    inter = torch.full((w.max_slots, w.n_inter, w.nv, w.K, w.V), float("nan"), device=DEV)
+    out = d.snapshots(inter, w.steps_per_token)
+    torch.cuda.synchronize()
+    sub_rows = [0, 1, 2]  # oracle on a sample of requests
+    sub = sub_workload(w, sub_rows)
+    p = problem(sub, state=pool.copy())
+    oint = np.full((w.max_slots, w.n_inter, w.nv, w.K, w.V), np.nan, np.float32)
+    ref = oracle.fwd_snapshots(p, oint, w.steps_per_token)
+    toks = np.concatenate([np.arange(w.offsets[b], w.offsets[b + 1]) for b in sub_rows])
+    err = np.abs(out.cpu().numpy()[toks].astype(np.float64) - ref).max()
+    assert err <= 2e-3, err
+    slots = [int(w.slot_idx[b]) for b in sub_rows]
+    host_inter = inter.cpu().numpy()
+    check_state(host_inter, oint, slots=slots)
+    check_state(pool_to_host(d.state), p.state, slots=slots)
+    # snapshots exist exactly for the live slots
+    live = set(w.live_slots())
+    for s in range(w.max_slots):
+        assert np.isnan(host_inter[s]).all() == (s not in live)
+    # rollback
+    acc = torch.from_numpy(w.accepted).to(DEV)
+    gdr.gdr_rollback(d.state, d.slot, inter, acc)
+    torch.cuda.synchronize()
+    host = pool_to_host(d.state)
+    for b in range(w.batch):
+        s = int(w.slot_idx[b])
+        assert (host[s] == host_inter[s, w.accepted[b]]).all()
+
+
+def test_snapshot_small_bf16_against_oracle():
+    w = W.random_case(500, [8, 7, 8, 3], nk=2, nv=4, K=32, max_slots=6, state_dtype="bf16",
+                      n_pad=1, decay_is_log=True)
+    pool = w.state_pool()
+    d = Dev(w, pool)
+    inter = torch.zeros((w.max_slots, 4, w.nv, w.K, w.V), dtype=torch.bfloat16, device=DEV)
+    out = d.snapshots(inter, 2)
+    p = problem(w, state=pool.copy())
+    oint = np.zeros((w.max_slots, 4, w.nv, w.K, w.V), np.uint16)
+    ref = oracle.fwd_snapshots(p, oint, 2)
+    check_out(out, ref)
+    check_state(pool_to_host(inter), oint)
+    check_state(pool_to_host(d.state), p.state)

@@ -18,7 +18,13 @@ from ._binding import (  # noqa: F401
     gdr_ring_record_elements,
     gdr_rollback,
     gdr_verify_ring,
+    Prepared,
     load_library,
+    prepare_fold,
+    prepare_fwd,
+    prepare_fwd_snapshots,
+    prepare_rollback,
+    prepare_verify_ring,
     status_names,
 )
 

@@ -289,3 +289,85 @@ def gdr_get_status(clear: bool = True) -> int:
 
 def status_names(bits: int):
     return [n for b, n in STATUS_BITS.items() if bits & b]
+
+
+class Prepared:
+    """A C-ABI call with its arguments marshalled once.
+
+    Calling it re-issues the same entry point on the same device buffers with
+    no per-call Python marshalling (the buffers' contents may change between
+    calls; their addresses, shapes and strides may not).  Useful for repeated
+    decode steps and for capturing the call into a CUDA graph."""
+
+    def __init__(self, fn, args: gdr_step_args, extra, keep, device):
+        self._fn = fn
+        self._args = args
+        self._extra = extra
+        self._keep = keep  # tensors whose storage the call uses
+        self._device = device
+
+    def __call__(self, stream: Optional[int] = None):
+        s = _stream(self._device) if stream is None else stream
+        _check(self._fn(ctypes.byref(self._args), *self._extra, s))
+
+
+def prepare_fwd(qkv, decay, beta, state, slot_idx, offsets, out, *, decay_is_log=False,
+                use_qk_l2norm=True, scale=0.0, eps=1e-6, max_row_len=0) -> Prepared:
+    a = make_args(qkv, decay, beta, state, slot_idx, offsets, out, nk=_nk_from_qkv(qkv, state),
+                  decay_is_log=decay_is_log, use_qk_l2norm=use_qk_l2norm, scale=scale, eps=eps,
+                  max_row_len=max_row_len)
+    return Prepared(load_library().gdr_fwd, a, (),
+                    (qkv, decay, beta, state, slot_idx, offsets, out), qkv.device)
+
+
+def prepare_verify_ring(qkv, decay, beta, state, slot_idx, offsets, ring, ring_slot_idx, out, *,
+                        decay_is_log=False, use_qk_l2norm=True, scale=0.0, eps=1e-6,
+                        max_row_len=0) -> Prepared:
+    _dev(ring, "ring", torch.float32)
+    _dev(ring_slot_idx, "ring_slot_idx", torch.int32)
+    if ring.dim() != 4 or not ring.is_contiguous():
+        raise ValueError("ring must be a contiguous [ring_rows, nk, ring_len, record_stride] tensor")
+    a = make_args(qkv, decay, beta, state, slot_idx, offsets, out, nk=_nk_from_qkv(qkv, state),
+                  decay_is_log=decay_is_log, use_qk_l2norm=use_qk_l2norm, scale=scale, eps=eps,
+                  max_row_len=max_row_len)
+    extra = (ring.data_ptr(), GDR_F32, ring.shape[0], ring.shape[2], ring.shape[3],
+             ring_slot_idx.data_ptr())
+    return Prepared(load_library().gdr_verify_ring, a, extra,
+                    (qkv, decay, beta, state, slot_idx, offsets, out, ring, ring_slot_idx),
+                    qkv.device)
+
+
+def prepare_fold(state, slot_idx, ring, ring_slot_idx, counts) -> Prepared:
+    _dev(ring, "ring", torch.float32)
+    _dev(ring_slot_idx, "ring_slot_idx", torch.int32)
+    _dev(counts, "counts", torch.int32)
+    if ring.dim() != 4 or not ring.is_contiguous():
+        raise ValueError("ring must be a contiguous [ring_rows, nk, ring_len, record_stride] tensor")
+    a = make_args(None, None, None, state, slot_idx, None, None, nk=ring.shape[1])
+    extra = (ring.data_ptr(), GDR_F32, ring.shape[0], ring.shape[2], ring.shape[3],
+             ring_slot_idx.data_ptr(), counts.data_ptr())
+    return Prepared(load_library().gdr_fold, a, extra,
+                    (state, slot_idx, ring, ring_slot_idx, counts), state.device)
+
+
+def prepare_fwd_snapshots(qkv, decay, beta, state, slot_idx, offsets, inter, steps_per_token, out,
+                          *, decay_is_log=False, use_qk_l2norm=True, scale=0.0, eps=1e-6,
+                          max_row_len=0) -> Prepared:
+    _dev(inter, "intermediate_states")
+    ss, st, sh, n_inter = _inter_strides(inter, state)
+    a = make_args(qkv, decay, beta, state, slot_idx, offsets, out, nk=_nk_from_qkv(qkv, state),
+                  decay_is_log=decay_is_log, use_qk_l2norm=use_qk_l2norm, scale=scale, eps=eps,
+                  max_row_len=max_row_len)
+    extra = (inter.data_ptr(), ss, st, sh, n_inter, int(steps_per_token))
+    return Prepared(load_library().gdr_fwd_snapshots, a, extra,
+                    (qkv, decay, beta, state, slot_idx, offsets, out, inter), qkv.device)
+
+
+def prepare_rollback(state, slot_idx, inter, accepted) -> Prepared:
+    _dev(inter, "intermediate_states")
+    _dev(accepted, "accepted", torch.int32)
+    ss, st, sh, n_inter = _inter_strides(inter, state)
+    a = make_args(None, None, None, state, slot_idx, None, None, nk=1)
+    extra = (inter.data_ptr(), ss, st, sh, n_inter, accepted.data_ptr())
+    return Prepared(load_library().gdr_rollback, a, extra, (state, slot_idx, inter, accepted),
+                    state.device)

@@ -160,3 +160,22 @@ __device__ __forceinline__ float gdr_advance(float s, float kh, float u, float a
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
 }  // namespace gdr
+
+namespace gdr {
+
+// ---- cp.async (LDGSTS): asynchronous global -> shared copies ---------------
+// Completion is awaited with cp.async.wait_group, a hardware wait (no spin loop).
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+}  // namespace gdr

@@ -245,3 +245,48 @@ def test_device_status_flags_bad_inputs():
     st = gdr.gdr_get_status(clear=True)
     assert st & 0x10, gdr.status_names(st)
     assert gdr.gdr_get_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
+def test_pipelined_decode_equals_simple_decode(state_dtype):
+    """Unit-stride, aligned q/k/v rows take the pipelined decode kernel; a
+    misaligned view of the same values takes the simple one: same bits."""
+    w = W.decode(batch=96, max_slots=192, state_dtype=state_dtype)
+    pool = w.state_pool()
+    o1, s1 = _run_fwd(w, pool, max_row_len=1)
+    d = Dev(w, pool)
+    T, C = w.qkv.shape
+    buf = torch.zeros(T * C + 1, device=DEV)
+    buf[1:] = torch.from_numpy(w.qkv).to(DEV).reshape(-1)
+    qkv = buf[1:].view(T, C)  # base 4 bytes past a 16-byte boundary
+    out = gdr.gdr_fwd(qkv, d.decay, d.beta, d.state, d.slot, d.off, max_row_len=1)
+    torch.cuda.synchronize()
+    assert (out.cpu().numpy().view(np.uint32) == o1.view(np.uint32)).all()
+    assert (pool_to_host(d.state) == s1).all()
+
+
+def test_decode_kernel_device_checks():
+    w = W.decode(batch=40, max_slots=64)
+    pool = w.state_pool()
+    slots = w.slot_idx.copy()
+    live = np.flatnonzero(slots >= 0)
+    slots[live[0]] = 1000  # beyond max_slots
+    bad = dataclasses.replace(w, slot_idx=slots)
+    d = Dev(bad, pool)
+    out = torch.full((w.total_tokens, w.nv * w.V), float("nan"), device=DEV)
+    d.fwd(max_row_len=1, out=out)
+    st = gdr.gdr_get_status(clear=True)
+    assert st & 0x1, gdr.status_names(st)
+    b = int(live[0])
+    assert (out[b] == 0).all()
+    assert not torch.isnan(out).any()
+    # a row of two tokens under max_row_len=1 is skipped and flagged
+    offs = np.concatenate([[0], np.arange(2, w.batch + 1)]).astype(np.int32)  # row 0 has 2 tokens
+    two = dataclasses.replace(w, offsets=offs, slot_idx=w.slot_idx[:-1].copy())
+    d = Dev(two, pool)
+    d.fwd(max_row_len=1)
+    st = gdr.gdr_get_status(clear=True)
+    assert st & 0x10, gdr.status_names(st)
+    s0 = int(two.slot_idx[0])
+    if s0 >= 0:
+        assert (pool_to_host(d.state)[s0] == pool[s0]).all()

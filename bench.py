@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--impl", default="gdr", choices=["gdr", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "verify_fold", "gdp_snapshots"], default=None,
+                    help="time just this secondary workload and print its figures (profiling aid)")
     ap.add_argument("--soak-s", type=float, default=1.0,
                     help="seconds of untimed steps after warm-up (steady clocks)")
     return ap.parse_args()
@@ -232,37 +234,38 @@ def time_steps(fn, steps, flush, stream):
     return [a.elapsed_time(b) for a, b in evs]
 
 
-def secondary(dev, flush, stream, hbm_peak, steps):
-    """Prefill, verify+fold and GDP snapshot+rollback workloads, timed like decode."""
+def _to_dev(x, dev):
+    import torch
+    return torch.from_numpy(x).to(dev)
+
+
+def _pool_dev(w, dev):
     import numpy as np
+    import torch
+    pool = w.state_pool(w.live_slots())
+    if pool.dtype == np.uint16:
+        return torch.from_numpy(pool.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(pool).to(dev)
+
+
+def bench_prefill(dev, flush, stream, hbm_peak, steps):
+    """Ragged prefill (FP32-FMA bound): rows of 512..4096 tokens."""
     import torch
     import gated_deltanet_linear_gdr_gb300 as gdr
     from gated_deltanet_linear_gdr_gb300 import workloads as W
-    props = torch.cuda.get_device_properties(dev)
-    res = {}
-
-    def t(x):
-        return torch.from_numpy(x).to(dev)
-
-    def pool_dev(w):
-        pool = w.state_pool(w.live_slots())
-        if pool.dtype == np.uint16:
-            return torch.from_numpy(pool.view(np.int16)).to(dev).view(torch.bfloat16)
-        return torch.from_numpy(pool).to(dev)
-
-    # --- ragged prefill (FP32-FMA bound)
     w = W.prefill()
-    st = pool_dev(w)
-    qkv, dec, bet, slot, off = t(w.qkv), t(w.decay), t(w.beta), t(w.slot_idx), t(w.offsets)
+    st = _pool_dev(w, dev)
+    qkv, dec, bet, slot, off = (_to_dev(x, dev) for x in (w.qkv, w.decay, w.beta, w.slot_idx, w.offsets))
     out = torch.empty((w.total_tokens, w.nv * w.V), device=dev)
     fn = gdr.prepare_fwd(qkv, dec, bet, st, slot, off, out)
     for _ in range(2):
         fn()
     ms = statistics.median(time_steps(fn, max(3, steps // 10), flush, stream))
     ht = w.live_head_tokens
+    props = torch.cuda.get_device_properties(dev)
     clk = props.clock_rate * 1e3 if hasattr(props, "clock_rate") else 2.07e9
     fp32_peak = props.multi_processor_count * 128 * clk
-    res["prefill"] = {
+    return {
         "workload": f"ragged prefill: {w.batch} rows, lengths {w.row_lengths.min()}..{w.row_lengths.max()}"
                     f" (T={w.total_tokens}), nk=16, nv=32, K=V=128, bf16 pool [16,32,128,128]",
         "ms": ms, "head_tokens_per_s": ht / (ms * 1e-3),
@@ -271,25 +274,33 @@ def secondary(dev, flush, stream, hbm_peak, steps):
         "frac_fp32_fma": fma_ops(ht, w.K, w.V) / (ms * 1e-3) / fp32_peak,
         "hbm_gbs": decode_bytes(w, 2) / (ms * 1e-3) / 1e9,
     }
-    del st, qkv, dec, bet, out
 
-    # --- speculative verify + fold (bf16 pool, fp32 ring)
+
+def bench_verify_fold(dev, flush, stream, hbm_peak, steps):
+    """Speculative verify (bf16 pool, fp32 ring of RING_LEN 8) then fold."""
+    import torch
+    import gated_deltanet_linear_gdr_gb300 as gdr
+    from gated_deltanet_linear_gdr_gb300 import workloads as W
     w = W.verify_fold()
-    st = pool_dev(w)
-    qkv, dec, bet, slot, off = t(w.qkv), t(w.decay), t(w.beta), t(w.slot_idx), t(w.offsets)
+    st = _pool_dev(w, dev)
+    qkv, dec, bet, slot, off = (_to_dev(x, dev) for x in (w.qkv, w.decay, w.beta, w.slot_idx, w.offsets))
     stride = (gdr.gdr_ring_record_elements(w.K, w.V, w.nv // w.nk) + 3) // 4 * 4
     ring = torch.zeros((w.ring_rows, w.nk, w.ring_len, stride), device=dev)
-    rsi, cnt = t(w.ring_slot_idx), t(w.counts)
+    rsi, cnt = _to_dev(w.ring_slot_idx, dev), _to_dev(w.counts, dev)
     out = torch.empty((w.total_tokens, w.nv * w.V), device=dev)
-    v_fn = gdr.prepare_verify_ring(qkv, dec, bet, st, slot, off, ring, rsi, out)
+    # the caller of a verify window knows its longest row: the short-row kernel
+    v_fn = gdr.prepare_verify_ring(qkv, dec, bet, st, slot, off, ring, rsi, out,
+                                   max_row_len=int(w.row_lengths.max()))
     f_fn = gdr.prepare_fold(st, slot, ring, rsi, cnt)
     for _ in range(2):
-        v_fn(); f_fn()  # noqa: E702
+        v_fn()
+        f_fn()
     tv = statistics.median(time_steps(v_fn, steps, flush, stream))
     tf = statistics.median(time_steps(f_fn, steps, flush, stream))
     L = w.row_lengths
     short = L <= w.ring_len
-    rec = w.K + ((w.nv // w.nk + 3) // 4) * 4 + (w.nv // w.nk) * w.V
+    r = w.nv // w.nk
+    rec = w.K + ((r + 3) // 4) * 4 + r * w.V
     conv = 2 * w.nk * w.K + w.nv * w.V
     vbytes = (w.batch * w.nv * w.K * w.V * 2 + int((~short).sum()) * w.nv * w.K * w.V * 2
               + w.total_tokens * (conv + 2 * w.nv + w.nv * w.V) * 4
@@ -298,7 +309,7 @@ def secondary(dev, flush, stream, hbm_peak, steps):
     fbytes = (int(active.sum()) * w.nv * w.K * w.V * 2 * 2
               + int(w.counts[active].sum()) * w.nk * rec * 4)
     ht = w.live_head_tokens
-    res["verify_fold"] = {
+    return {
         "workload": "verify: 127 rows x 5 drafts + 1 row of 12, RING_LEN 8, nk=16, nv=32, "
                     "K=V=128, bf16 pool [256,32,128,128], fp32 ring [256,16,8,388]; then fold "
                     "of accepted counts ~U{0..5}",
@@ -306,26 +317,31 @@ def secondary(dev, flush, stream, hbm_peak, steps):
         "verify_hbm_gbs": vbytes / (tv * 1e-3) / 1e9, "fold_hbm_gbs": fbytes / (tf * 1e-3) / 1e9,
         "frac_hbm_verify_plus_fold": (vbytes + fbytes) / ((tv + tf) * 1e-3) / 1e9 / hbm_peak,
     }
-    del st, ring, qkv, out
 
-    # --- GDP snapshots + rollback (fp32 cache)
+
+def bench_gdp_snapshots(dev, flush, stream, hbm_peak, steps):
+    """Gated Delta Product drafts with snapshots (fp32 cache), then rollback."""
+    import torch
+    import gated_deltanet_linear_gdr_gb300 as gdr
+    from gated_deltanet_linear_gdr_gb300 import workloads as W
     w = W.gdp_snapshots()
-    st = pool_dev(w)
-    qkv, dec, bet, slot, off = t(w.qkv), t(w.decay), t(w.beta), t(w.slot_idx), t(w.offsets)
+    st = _pool_dev(w, dev)
+    qkv, dec, bet, slot, off = (_to_dev(x, dev) for x in (w.qkv, w.decay, w.beta, w.slot_idx, w.offsets))
     inter = torch.zeros((w.max_slots, w.n_inter, w.nv, w.K, w.V), device=dev)
-    acc = t(w.accepted)
+    acc = _to_dev(w.accepted, dev)
     out = torch.empty((w.total_tokens, w.nv * w.V), device=dev)
     s_fn = gdr.prepare_fwd_snapshots(qkv, dec, bet, st, slot, off, inter, w.steps_per_token, out,
-                                     decay_is_log=True)
+                                     decay_is_log=True, max_row_len=int(w.row_lengths.max()))
     r_fn = gdr.prepare_rollback(st, slot, inter, acc)
     for _ in range(2):
-        s_fn(); r_fn()  # noqa: E702
+        s_fn()
+        r_fn()
     ts = statistics.median(time_steps(s_fn, steps, flush, stream))
     tr = statistics.median(time_steps(r_fn, steps, flush, stream))
     sbytes = decode_bytes(w, 4) + w.batch * w.n_inter * w.nv * w.K * w.V * 4
     rbytes = w.batch * w.nv * w.K * w.V * 4 * 2
     ht = w.live_head_tokens
-    res["gdp_snapshots"] = {
+    return {
         "workload": "GDP spec-decode: 64 requests x 4 drafts x 2 Householder copies (T=8 each), "
                     "spt=2, nk=16, nv=32, K=V=128, fp32 cache [128,32,128,128], "
                     "intermediate [128,4,32,128,128]; then rollback",
@@ -334,8 +350,20 @@ def secondary(dev, flush, stream, hbm_peak, steps):
         "frac_hbm_snapshots": sbytes / (ts * 1e-3) / 1e9 / hbm_peak,
         "frac_hbm_rollback": rbytes / (tr * 1e-3) / 1e9 / hbm_peak,
     }
-    del st, inter, qkv, out
-    torch.cuda.empty_cache()
+
+
+SECONDARY = {"prefill": bench_prefill, "verify_fold": bench_verify_fold,
+             "gdp_snapshots": bench_gdp_snapshots}
+
+
+def secondary(dev, flush, stream, hbm_peak, steps, only=None):
+    """The non-headline workloads, each timed like decode (L2 flushed per step)."""
+    import torch
+    res = {}
+    for name, fn in SECONDARY.items():
+        if only is None or only == name:
+            res[name] = fn(dev, flush, stream, hbm_peak, steps)
+            torch.cuda.empty_cache()
     return res
 
 
@@ -374,6 +402,13 @@ def run_gdr(args):
     gdr.load_library()
     stream = torch.cuda.current_stream(dev)
 
+    if args.only:
+        props = torch.cuda.get_device_properties(dev)
+        flush_buf = torch.zeros(max(2 * getattr(props, "L2_cache_size", 128 << 20), 256 << 20) // 4,
+                                dtype=torch.float32, device=dev)
+        res = secondary(dev, lambda: flush_buf.sum(), stream, peaks()[0], args.steps, only=args.only)
+        print(json.dumps({"only": args.only, **res.get(args.only, {})}), flush=True)
+        return
     w = W.decode(seed=1 + rank)
     step = DecodeStep(w, dev)
     props = torch.cuda.get_device_properties(dev)

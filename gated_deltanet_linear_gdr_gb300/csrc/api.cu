@@ -144,6 +144,21 @@ gdr::StepParams lower(const gdr_step_args *a, unsigned *status) {
     return p;
 }
 
+// Rows of at most this many tokens (by the caller's max_row_len promise) run on
+// the pipelined short-row kernel; longer or unknown lengths on the general one.
+constexpr long long kShortRowMax = 64;
+
+cudaError_t launch_rows(const gdr::StepParams &p, const gdr_step_args *a, gdr::Mode mode, const gdr::RingParams &rp,
+                        const gdr::SnapParams &sp, cudaStream_t s) {
+    const bool bf16 = a->state_dtype == GDR_BF16;
+    if (a->max_row_len >= 1 && a->max_row_len <= kShortRowMax) {
+        bool used = false;
+        cudaError_t e = gdr::launch_short(p, a->K, bf16, mode, rp, sp, a->max_row_len, s, &used);
+        if (used || e != cudaSuccess) return e;
+    }
+    return gdr::launch_chain(p, a->K, bf16, mode, rp, sp, a->max_row_len, s);
+}
+
 int launched(cudaError_t e, const char *fn) {
     if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
     return ok();
@@ -209,9 +224,7 @@ int gdr_fwd(const gdr_step_args *a, void *stream) {
     const gdr::StepParams p = lower(a, st);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (a->max_row_len == 1) return launched(gdr::launch_decode(p, a->K, a->state_dtype == GDR_BF16, s), "gdr_fwd");
-    return launched(gdr::launch_chain(p, a->K, a->state_dtype == GDR_BF16, gdr::Mode::Fwd, gdr::RingParams{},
-                                      gdr::SnapParams{}, a->max_row_len, s),
-                    "gdr_fwd");
+    return launched(launch_rows(p, a, gdr::Mode::Fwd, gdr::RingParams{}, gdr::SnapParams{}, s), "gdr_fwd");
 }
 
 int gdr_verify_ring(const gdr_step_args *a, float *ring, int32_t ring_dtype, int64_t ring_rows,
@@ -234,8 +247,7 @@ int gdr_verify_ring(const gdr_step_args *a, float *ring, int32_t ring_dtype, int
     rp.ring_slot = ring_slot_idx;
     rp.alpha_off = a->K;
     rp.u_off = a->K + ((r + 3) / 4) * 4;
-    return launched(gdr::launch_chain(p, a->K, a->state_dtype == GDR_BF16, gdr::Mode::Verify, rp,
-                                      gdr::SnapParams{}, a->max_row_len, static_cast<cudaStream_t>(stream)),
+    return launched(launch_rows(p, a, gdr::Mode::Verify, rp, gdr::SnapParams{}, static_cast<cudaStream_t>(stream)),
                     "gdr_verify_ring");
 }
 
@@ -294,8 +306,7 @@ int gdr_fwd_snapshots(const gdr_step_args *a, void *inter, int64_t inter_slot_st
     sp.s_head = inter_head_stride;
     sp.n_inter = n_inter;
     sp.spt = steps_per_token;
-    return launched(gdr::launch_chain(p, a->K, a->state_dtype == GDR_BF16, gdr::Mode::Snap, gdr::RingParams{}, sp,
-                                      a->max_row_len, static_cast<cudaStream_t>(stream)),
+    return launched(launch_rows(p, a, gdr::Mode::Snap, gdr::RingParams{}, sp, static_cast<cudaStream_t>(stream)),
                     "gdr_fwd_snapshots");
 }
 

@@ -159,6 +159,60 @@ __device__ __forceinline__ float gdr_advance(float s, float kh, float u, float a
 
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
+// ---- the same operations on pairs of columns --------------------------------
+// Blackwell's packed f32x2 FMA / MUL round each element exactly like the
+// scalar instruction, so these are bit-identical to the scalar helpers above
+// and issue half as many instructions.  x[] holds C consecutive columns.
+template <int C>
+__device__ __forceinline__ void chain_first_cols(const float (&s)[C], float k, float (&p)[C]) {
+    if constexpr (C % 2 == 0) {
+        const float2 kk = make_float2(k, k);
+#pragma unroll
+        for (int j = 0; j < C; j += 2) {
+            const float2 r = __fmul2_rn(make_float2(s[j], s[j + 1]), kk);
+            p[j] = r.x;
+            p[j + 1] = r.y;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < C; ++j) p[j] = chain_first(s[j], k);
+    }
+}
+
+template <int C>
+__device__ __forceinline__ void chain_next_cols(const float (&s)[C], float k, float (&p)[C]) {
+    if constexpr (C % 2 == 0) {
+        const float2 kk = make_float2(k, k);
+#pragma unroll
+        for (int j = 0; j < C; j += 2) {
+            const float2 r = __ffma2_rn(make_float2(s[j], s[j + 1]), kk, make_float2(p[j], p[j + 1]));
+            p[j] = r.x;
+            p[j + 1] = r.y;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < C; ++j) p[j] = chain_next(s[j], k, p[j]);
+    }
+}
+
+// s[j] <- kh * u[j] + alpha * s[j] for C columns (gdr_advance on each).
+template <int C>
+__device__ __forceinline__ void advance_cols(float (&s)[C], float kh, const float (&u)[C], float alpha) {
+    if constexpr (C % 2 == 0) {
+        const float2 kk = make_float2(kh, kh), aa = make_float2(alpha, alpha);
+#pragma unroll
+        for (int j = 0; j < C; j += 2) {
+            const float2 r =
+                __ffma2_rn(kk, make_float2(u[j], u[j + 1]), __fmul2_rn(aa, make_float2(s[j], s[j + 1])));
+            s[j] = r.x;
+            s[j + 1] = r.y;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < C; ++j) s[j] = gdr_advance(s[j], kh, u[j], alpha);
+    }
+}
+
 }  // namespace gdr
 
 namespace gdr {

@@ -189,15 +189,12 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
 #pragma unroll
                 for (int ii = 0; ii < 4; ++ii) {
                     const int r = g * 8 + i4 * 4 + ii;
-#pragma unroll
-                    for (int c = 0; c < C; ++c) {
-                        if (i4 == 0 && ii == 0) {
-                            pa[g][c] = chain_first(s[r][c], knv[ii]);
-                            pb[g][c] = chain_first(s[r][c], qnv[ii]);
-                        } else {
-                            pa[g][c] = chain_next(s[r][c], knv[ii], pa[g][c]);
-                            pb[g][c] = chain_next(s[r][c], qnv[ii], pb[g][c]);
-                        }
+                    if (i4 == 0 && ii == 0) {
+                        chain_first_cols<C>(s[r], knv[ii], pa[g]);
+                        chain_first_cols<C>(s[r], qnv[ii], pb[g]);
+                    } else {
+                        chain_next_cols<C>(s[r], knv[ii], pa[g]);
+                        chain_next_cols<C>(s[r], qnv[ii], pb[g]);
                     }
                 }
             }
@@ -255,16 +252,13 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
 #pragma unroll
                     for (int ii = 0; ii < 4; ++ii) {
                         const int r = g * 8 + i4 * 4 + ii;
-#pragma unroll
-                        for (int c = 0; c < C; ++c) {
-                            s[r][c] = gdr_advance(s[r][c], kcv[ii], u[c], alpha);
-                            if (i4 == 0 && ii == 0) {
-                                pa[g][c] = chain_first(s[r][c], knv[ii]);
-                                pb[g][c] = chain_first(s[r][c], qnv[ii]);
-                            } else {
-                                pa[g][c] = chain_next(s[r][c], knv[ii], pa[g][c]);
-                                pb[g][c] = chain_next(s[r][c], qnv[ii], pb[g][c]);
-                            }
+                        advance_cols<C>(s[r], kcv[ii], u, alpha);
+                        if (i4 == 0 && ii == 0) {
+                            chain_first_cols<C>(s[r], knv[ii], pa[g]);
+                            chain_first_cols<C>(s[r], qnv[ii], pb[g]);
+                        } else {
+                            chain_next_cols<C>(s[r], knv[ii], pa[g]);
+                            chain_next_cols<C>(s[r], qnv[ii], pb[g]);
                         }
                     }
                 }

@@ -9,7 +9,7 @@
 // no shared memory and no block barrier is needed, and every warp streams its
 // 128-row x 16-column bf16 tile (4 KiB) in and out once.  The state stays in
 // its storage format in registers and is widened on use.
-#include "gdr_device.cuh"
+#include "gdr_pipe.cuh"
 
 namespace gdr {
 
@@ -139,91 +139,24 @@ __global__ void __launch_bounds__(kDecodeThreads) k_decode(const StepParams p) {
 
 // ---------------------------------------------------------------------------
 // Pipelined variant for the common layouts (16-byte state vectors, unit-stride
-// Q/K/V rows).  Persistent CTAs walk units = (row, value head, CW-column tile)
-// with a stride of gridDim.x.  While a unit is computed, the next unit's state
-// tile and operands are already in flight into the other shared-memory stage
-// through cp.async, so every SM keeps tens of KiB of loads outstanding.  The
-// state tile is stored with the 16-byte chunk index XOR-ed by (row / 8), which
-// makes the warp-layout reads below free of bank conflicts.  The arithmetic is
-// the same sequence of operations as k_decode.
-template <typename ST, int K> struct PipeShape {
-    static constexpr int V = K;
-    static constexpr int LK = K / 8;
-    static constexpr int LV = 32 / LK;
-    static constexpr int C = 16 / (int)sizeof(ST);          // one 16-byte vector per row
-    static constexpr bool OK = C <= V / LV;
-    static constexpr int WC = LV * C;                       // columns per warp
-    static constexpr int NW = OK ? cmin(8, V / WC) : 1;      // warps per CTA
-    static constexpr int NT = 32 * NW;
-    static constexpr int CW = NW * WC;                      // columns per unit
-    static constexpr int USL = V / CW;                      // units per (row, head)
-    static constexpr int CPR = CW * (int)sizeof(ST) / 16;   // 16-byte chunks per tile row
-    static constexpr int S_STATE = K * CPR;                 // stage layout, in 16-byte chunks
-    static constexpr int S_Q = K / 4, S_K = K / 4, S_V = CW / 4;
-    static constexpr int SC = S_STATE + S_Q + S_K + S_V + 1;
-    static constexpr int SMEM1 = SC * 16;                   // bytes per stage
-};
+// Q/K/V rows).  Persistent CTAs walk (row, value head, tile) units with a
+// stride of gridDim.x; NS shared-memory stages keep NS-1 units' copies in
+// flight while one is computed.  Same arithmetic as k_decode.
 
-// What a CTA needs to know about one unit.  hu = h * USL + us; a unit past the
-// end of the batch is an empty row (t0 == t1 == 0).
-struct UnitMeta {
-    int hu, t0, t1, slot;
-};
-
-// Unit index -> (row b, head h, tile us), us fastest; 32-bit arithmetic.
-template <int USL>
-__device__ __forceinline__ UnitMeta unit_meta(const StepParams &p, int u, int nunits) {
-    UnitMeta m{};
-    if (u >= nunits) return m;
-    const int bh = u / USL;
-    const int b = bh / p.nv;
-    m.hu = u - b * p.nv * USL;
-    m.t0 = p.offsets[b];
-    m.t1 = p.offsets[b + 1];
-    m.slot = p.slot_idx[b];
-    return m;
-}
-
-__device__ __forceinline__ bool unit_streams(const StepParams &p, const UnitMeta &m) {
+__device__ __forceinline__ bool decode_unit_streams(const StepParams &p, const UnitMeta &m) {
     return m.t0 >= 0 && m.t1 == m.t0 + 1 && m.t1 <= p.T && m.slot >= 0 && m.slot < p.max_slots;
 }
-
-// Per-thread share of a tile copy: chunk j (j < NJ) of this thread is tile row
-// r0 + j*RPI, 16-byte column chunk c0; its shared-memory slot is swizzled.
-template <typename ST, int K> struct TileLane {
-    using Sh = PipeShape<ST, K>;
-    static constexpr int CPR = Sh::CPR;
-    static constexpr int RPI = Sh::NT / CPR;
-    static constexpr int NJ = Sh::S_STATE / Sh::NT;
-    static_assert(Sh::NT % CPR == 0 && Sh::S_STATE % Sh::NT == 0, "tile split");
-    int r0, c0;
-    long long goff;  // element offset of chunk 0 inside the (slot, head) block
-    long long gstep; // element offset between consecutive chunks of this thread
-    __device__ __forceinline__ void init(const StepParams &p) {
-        r0 = threadIdx.x / CPR;
-        c0 = threadIdx.x % CPR;
-        goff = (long long)r0 * p.st_k + c0 * (16 / (int)sizeof(ST));
-        gstep = (long long)RPI * p.st_k;
-    }
-    __device__ __forceinline__ int soff(int j) const {
-        const int row = r0 + j * RPI;
-        return row * CPR + (c0 ^ ((row >> 3) & (CPR - 1)));
-    }
-};
 
 // Queue the copies of one unit into a stage (always commits one group).
 template <typename ST, int K>
 __device__ __forceinline__ void unit_issue(const StepParams &p, const UnitMeta &m, uint4 *stage) {
     using Sh = PipeShape<ST, K>;
-    if (unit_streams(p, m)) {
-        TileLane<ST, K> tl;  // recomputed per unit: cheaper than keeping it live
-        tl.init(p);
+    if (decode_unit_streams(p, m)) {
         const int tid = threadIdx.x;
         const int h = m.hu / Sh::USL, us = m.hu % Sh::USL;
-        const ST *src = reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
-                        (long long)h * p.st_head + us * Sh::CW + tl.goff;
-#pragma unroll
-        for (int j = 0; j < TileLane<ST, K>::NJ; ++j) cp_async16(stage + tl.soff(j), src + j * tl.gstep);
+        tile_issue<ST, K>(reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
+                              (long long)h * p.st_head + us * Sh::CW,
+                          p.st_k, stage);
         const int hk = h / p.r;
         const float *trow = p.qkv + (long long)m.t0 * p.qkv_ss;
         for (int ch = tid; ch < Sh::S_Q + Sh::S_K + Sh::S_V; ch += Sh::NT) {
@@ -285,7 +218,6 @@ __device__ __forceinline__ void unit_compute(const StepParams &p, const UnitMeta
         q[i] = a4.x; q[i + 1] = a4.y; q[i + 2] = a4.z; q[i + 3] = a4.w;
         k[i] = b4.x; k[i + 1] = b4.y; k[i + 2] = b4.z; k[i + 3] = b4.w;
     }
-
     float ssq = chain_first(q[0], q[0]), ssk = chain_first(k[0], k[0]), kqr = chain_first(k[0], q[0]);
 #pragma unroll
     for (int i = 1; i < 8; ++i) {
@@ -303,62 +235,33 @@ __device__ __forceinline__ void unit_compute(const StepParams &p, const UnitMeta
         k[i] = __fmul_rn(k[i], inv_k);  // k^
         q[i] = __fmul_rn(q[i], qsc);    // q~
     }
-    // Rows 8*kl .. 8*kl+7 share the swizzle (row / 8 == kl), so this lane's
-    // chunk of row 8*kl + i sits at a fixed base plus i*CPR.
-    uint4 *mine = stage + kl * 8 * CPR + ((col / C) ^ (kl & (CPR - 1)));
+    uint4 *mine = tile_lane_base<ST, K>(stage, kl, col);
     float a[C], bq[C];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         Pack<ST, C> x;
         x.u.v = *reinterpret_cast<const VT *>(mine + i * CPR);
+        float sr[C];
 #pragma unroll
-        for (int c = 0; c < C; ++c) {
-            const float s = x.get(c);
-            a[c] = i == 0 ? chain_first(s, k[i]) : chain_next(s, k[i], a[c]);
-            bq[c] = i == 0 ? chain_first(s, q[i]) : chain_next(s, q[i], bq[c]);
+        for (int c = 0; c < C; ++c) sr[c] = x.get(c);
+        if (i == 0) {
+            chain_first_cols<C>(sr, k[0], a);
+            chain_first_cols<C>(sr, q[0], bq);
+        } else {
+            chain_next_cols<C>(sr, k[i], a);
+            chain_next_cols<C>(sr, q[i], bq);
         }
     }
     const float alpha = gdr_alpha(ab[0], p.decay_is_log);
     const float beta = ab[1];
     float u[C];
     if constexpr (LK == 2 * C) {
-        // Reduce-scatter over the LK lanes of a column group: at the level that
-        // pairs lanes (l, l^m) each lane keeps half of its values and adds the
-        // partner's partials for them -- the same pairwise tree as tree_lanes,
-        // in 2C-1 shuffles instead of 2C*log2(LK).  Lane kl ends with value
-        // j = bit-reverse(kl) of [a_0..a_{C-1}, b_0..b_{C-1}].
-        float x[2 * C];
-#pragma unroll
-        for (int c = 0; c < C; ++c) {
-            x[c] = a[c];
-            x[C + c] = bq[c];
-        }
-#pragma unroll
-        for (int m = 1, n = 2 * C; m < LK; m <<= 1, n >>= 1) {
-            const bool hi = (kl & m) != 0;
-#pragma unroll
-            for (int i = 0; i < n / 2; ++i) {
-                const float send = hi ? x[i] : x[n / 2 + i];
-                const float keep = hi ? x[n / 2 + i] : x[i];
-                x[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, m));
-            }
-        }
-        // lane pair (kl, kl^1) holds (a_c, b_c) with c = bits 1..3 of kl reversed
-        int c = 0;
-#pragma unroll
-        for (int m = 2, w = C / 2; m < LK; m <<= 1, w >>= 1) c += (kl & m) ? w : 0;
-        const float other = __shfl_xor_sync(kFull, x[0], 1);
-        const float A = (kl & 1) ? other : x[0];
-        const float B = (kl & 1) ? x[0] : other;
+        float A, B;
+        rs_reduce<LK, C>(a, bq, kl, A, B);
+        const int c = rs_column<LK, C>(kl);
         const float uc = gdr_u(beta, alpha, A, vs[col + c]);
         if (!(kl & 1)) orow[(long long)c * p.out_vs] = gdr_o(alpha, B, kq, uc);
-#pragma unroll
-        for (int cc = 0; cc < C; ++cc) {
-            int src = 0;
-#pragma unroll
-            for (int m = 2, w = C / 2; m < LK; m <<= 1, w >>= 1) src |= (cc & w) ? m : 0;
-            u[cc] = __shfl_sync(kFull, uc, (lane & ~(LK - 1)) | src);
-        }
+        rs_broadcast<LK, C>(uc, lane, u);
     } else {
 #pragma unroll
         for (int c = 0; c < C; ++c) {
@@ -370,45 +273,17 @@ __device__ __forceinline__ void unit_compute(const StepParams &p, const UnitMeta
         if (kl == 0) store_f32<C>(orow, p.out_vs, p.out_vec, a);
     }
     // New state back into the same (lane-private) chunks of the stage; the CTA
-    // then writes the whole tile to HBM with coalesced rows (unit_store).
+    // then writes the whole tile to HBM with coalesced rows.
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         Pack<ST, C> x;
         x.u.v = *reinterpret_cast<const VT *>(mine + i * CPR);
         float n[C];
 #pragma unroll
-        for (int c = 0; c < C; ++c) n[c] = gdr_advance(x.get(c), k[i], u[c], alpha);
-        if constexpr (sizeof(ST) == 2 && C % 2 == 0) {
-            // two round-to-nearest-even conversions per instruction (same bits as one at a time)
-            uint32_t w[C / 2];
-#pragma unroll
-            for (int j = 0; j < C / 2; ++j) {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(n[2 * j], n[2 * j + 1]);
-                w[j] = *reinterpret_cast<const uint32_t *>(&h2);
-            }
-            *reinterpret_cast<VT *>(mine + i * CPR) = *reinterpret_cast<const VT *>(w);
-        } else {
-#pragma unroll
-            for (int c = 0; c < C; ++c) x.set(c, n[c]);
-            *reinterpret_cast<VT *>(mine + i * CPR) = x.u.v;
-        }
+        for (int c = 0; c < C; ++c) n[c] = x.get(c);
+        advance_cols<C>(n, k[i], u, alpha);
+        pack_store<ST, C>(mine + i * CPR, n);
     }
-}
-
-// Coalesced write-back of a computed tile: consecutive threads store
-// consecutive 16-byte chunks of a row.
-template <typename ST, int K>
-__device__ __forceinline__ void unit_store(const StepParams &p, const UnitMeta &m, const uint4 *stage) {
-    using Sh = PipeShape<ST, K>;
-    if (!unit_streams(p, m)) return;
-    TileLane<ST, K> tl;
-    tl.init(p);
-    const int h = m.hu / Sh::USL, us = m.hu % Sh::USL;
-    ST *dst = reinterpret_cast<ST *>(p.state) + (long long)m.slot * p.st_slot + (long long)h * p.st_head +
-              us * Sh::CW + tl.goff;
-#pragma unroll
-    for (int j = 0; j < TileLane<ST, K>::NJ; ++j)
-        *reinterpret_cast<uint4 *>(dst + j * tl.gstep) = stage[tl.soff(j)];
 }
 
 template <typename ST, int K, int NS>
@@ -434,9 +309,15 @@ __global__ void __launch_bounds__(PipeShape<ST, K>::NT, NS == 2 ? 3 : 2)
         const UnitMeta later = unit_meta<Sh::USL>(p, ul < nunits ? (int)ul : nunits, nunits);
         cp_async_wait<NS - 1>();
         __syncthreads();
-        unit_compute<ST, K>(p, mq[0], smem_pipe + cur * Sh::SC);
+        uint4 *stage = smem_pipe + cur * Sh::SC;
+        unit_compute<ST, K>(p, mq[0], stage);
         __syncthreads();
-        unit_store<ST, K>(p, mq[0], smem_pipe + cur * Sh::SC);
+        if (decode_unit_streams(p, mq[0])) {
+            const int h = mq[0].hu / Sh::USL, us = mq[0].hu % Sh::USL;
+            tile_store<ST, K>(reinterpret_cast<ST *>(p.state) + (long long)mq[0].slot * p.st_slot +
+                                  (long long)h * p.st_head + us * Sh::CW,
+                              p.st_k, stage);
+        }
         __syncthreads();
 #pragma unroll
         for (int s = 0; s < NS - 1; ++s) mq[s] = mq[s + 1];

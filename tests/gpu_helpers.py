@@ -54,9 +54,9 @@ class Dev:
         return gdr.gdr_verify_ring(self.qkv, self.decay, self.beta, self.state, self.slot,
                                    self.off, ring, ring_slot, max_row_len=max_row_len, **self.kw)
 
-    def snapshots(self, inter, spt):
+    def snapshots(self, inter, spt, max_row_len=0):
         return gdr.gdr_fwd_snapshots(self.qkv, self.decay, self.beta, self.state, self.slot,
-                                     self.off, inter, spt, **self.kw)
+                                     self.off, inter, spt, max_row_len=max_row_len, **self.kw)
 
 
 def check_out(gpu_out: torch.Tensor, ref: np.ndarray, atol=OUT_ATOL):

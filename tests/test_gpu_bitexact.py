@@ -290,3 +290,71 @@ def test_decode_kernel_device_checks():
     s0 = int(two.slot_idx[0])
     if s0 >= 0:
         assert (pool_to_host(d.state)[s0] == pool[s0]).all()
+
+
+@pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
+def test_short_row_kernel_equals_general_kernel(state_dtype):
+    """The same rows through the short-row kernel (max_row_len hint) and the
+    general kernel: forward, verify (records and pool) and snapshots agree bit
+    for bit, including rows longer than one staged chunk."""
+    lengths = [5, 1, 8, 0, 12, 3, 20, 7]
+    w = W.random_case(700, lengths, nk=4, nv=8, K=128, max_slots=12, state_dtype=state_dtype,
+                      n_pad=1, decay_is_log=True)
+    pool = w.state_pool()
+    hint = max(lengths)
+    o1, s1 = _run_fwd(w, pool, max_row_len=hint)
+    o0, s0 = _run_fwd(w, pool, max_row_len=0)
+    assert (o1.view(np.uint32) == o0.view(np.uint32)).all()
+    assert (s1 == s0).all()
+    rsi = torch.arange(w.batch, dtype=torch.int32, device=DEV)
+    rings, outs, pools = [], [], []
+    for h in (hint, 0):
+        d = Dev(w, pool)
+        ring = ring_for(w, 8, w.batch)
+        outs.append(d.verify(ring, rsi, max_row_len=h).cpu().numpy())
+        rings.append(ring.cpu().numpy())
+        pools.append(pool_to_host(d.state))
+    assert (outs[0].view(np.uint32) == outs[1].view(np.uint32)).all()
+    assert (np.isnan(rings[0]) == np.isnan(rings[1])).all()
+    m = ~np.isnan(rings[0])
+    assert (rings[0][m].view(np.uint32) == rings[1][m].view(np.uint32)).all()
+    assert (pools[0] == pools[1]).all()
+    inters, pools = [], []
+    tdt = torch.bfloat16 if state_dtype == "bf16" else torch.float32
+    for h in (hint, 0):
+        d = Dev(w, pool)
+        inter = torch.zeros((w.max_slots, 6, w.nv, w.K, w.V), dtype=tdt, device=DEV)
+        d.snapshots(inter, 3, max_row_len=h)
+        inters.append(pool_to_host(inter))
+        pools.append(pool_to_host(d.state))
+    assert (inters[0] == inters[1]).all()
+    assert (pools[0] == pools[1]).all()
+    st = gdr.gdr_get_status(clear=True)
+    assert st == 0, gdr.status_names(st)  # the 20-token row has exactly n_inter = 6 drafts of 3
+
+
+@pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
+def test_pipelined_fold_equals_simple_fold(state_dtype):
+    """A 16-byte-aligned ring takes the pipelined fold, a view offset by one
+    float takes the simple one: same bits."""
+    w = W.verify_fold(batch=40, max_slots=64, ring_rows=64, state_dtype=state_dtype)
+    pool = w.state_pool()
+    d = Dev(w, pool)
+    ring = ring_for(w, w.ring_len, w.ring_rows)
+    rsi = torch.from_numpy(w.ring_slot_idx).to(DEV)
+    d.verify(ring, rsi, max_row_len=12)
+    cnt = torch.from_numpy(w.counts).to(DEV)
+    outs = []
+    for shifted in (False, True):
+        st = pool_to_dev(pool_to_host(d.state))
+        if shifted:
+            buf = torch.empty(ring.numel() + 1, device=DEV)
+            buf[1:] = ring.reshape(-1)
+            r = buf[1:].view(ring.shape)
+        else:
+            r = ring
+        gdr.gdr_fold(st, d.slot, r, rsi, cnt)
+        torch.cuda.synchronize()
+        outs.append(pool_to_host(st))
+    assert (outs[0] == outs[1]).all()
+    assert gdr.gdr_get_status(clear=True) == 0

@@ -47,13 +47,14 @@ def test_tiny_config():
 
 @pytest.mark.parametrize("K", [16, 32, 64, 128])
 @pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
-def test_ragged_rows_all_head_dims(K, state_dtype):
-    # lengths span several staged chunks (16 tokens) with ragged tails, plus empty
-    # and single-token rows and a padding row; GQA ratio 2
+@pytest.mark.parametrize("hint", [0, 40])  # 0: general kernel; 40: short-row kernel where it applies
+def test_ragged_rows_all_head_dims(K, state_dtype, hint):
+    # lengths span several staged chunks (8 and 16 tokens) with ragged tails, plus
+    # empty and single-token rows and a padding row; GQA ratio 2
     lengths = [37, 0, 1, 16, 5, 33]
     w = W.random_case(100 + K, lengths, nk=2, nv=4, K=K, max_slots=9, state_dtype=state_dtype,
                       n_pad=1)
-    _fwd_parity(w)
+    _fwd_parity(w, max_row_len=hint)
 
 
 @pytest.mark.parametrize("K", [16, 32, 64, 128])
@@ -118,13 +119,14 @@ def test_prefill_config_sampled_rows():
     check_state(host, p.state, slots=[int(w.slot_idx[b]) for b in rows])
 
 
-def test_verify_fold_config():
+@pytest.mark.parametrize("hint", [0, 12])  # 0: general kernel; 12: short-row kernel
+def test_verify_fold_config(hint):
     w = W.verify_fold()
     pool = w.state_pool()
     d = Dev(w, pool)
     ring = ring_for(w, w.ring_len, w.ring_rows)
     rsi = torch.from_numpy(w.ring_slot_idx).to(DEV)
-    out = d.verify(ring, rsi)
+    out = d.verify(ring, rsi, max_row_len=hint)
     torch.cuda.synchronize()
     pv = problem(w, state=pool.copy())
     oring = np.full(tuple(ring.shape), np.nan, np.float32)
@@ -177,7 +179,8 @@ def test_fold_on_synthetic_ring(state_dtype):
             assert (host[s] == pool[s]).all()
 
 
-def test_gdp_snapshot_config_and_rollback():
+@pytest.mark.parametrize("hint", [0, 8])  # 0: general kernel; 8: short-row kernel
+def test_gdp_snapshot_config_and_rollback(hint):
     """Gated Delta Product spec-decode at full size: 64 requests x 4 drafts x 2
     Householder copies, fp32 cache [128, 32, 128, 128], snapshots every 2 steps,
     then rollback to a random accepted draft."""
@@ -185,7 +188,7 @@ def test_gdp_snapshot_config_and_rollback():
     pool = w.state_pool()
     d = Dev(w, pool)
     inter = torch.full((w.max_slots, w.n_inter, w.nv, w.K, w.V), float("nan"), device=DEV)
-    out = d.snapshots(inter, w.steps_per_token)
+    out = d.snapshots(inter, w.steps_per_token, max_row_len=hint)
     torch.cuda.synchronize()
     sub_rows = [0, 1, 2]  # oracle on a sample of requests
     sub = sub_workload(w, sub_rows)

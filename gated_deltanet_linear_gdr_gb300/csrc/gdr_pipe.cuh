@@ -53,11 +53,11 @@ __device__ __forceinline__ UnitMeta unit_meta(const StepParams &p, int u, int nu
 // src, rows st_k elements apart) into shared memory, swizzled.  Every thread
 // of the CTA takes S_STATE / NT chunks; consecutive threads read consecutive
 // 16-byte chunks of a row.
-template <typename ST, int K>
+template <typename ST, int K, int NT = PipeShape<ST, K>::NT>
 __device__ __forceinline__ void tile_issue(const ST *src, long long st_k, uint4 *tile) {
     using Sh = PipeShape<ST, K>;
-    constexpr int CPR = Sh::CPR, RPI = Sh::NT / CPR, NJ = Sh::S_STATE / Sh::NT;
-    static_assert(Sh::NT % CPR == 0 && Sh::S_STATE % Sh::NT == 0, "tile split");
+    constexpr int CPR = Sh::CPR, RPI = NT / CPR, NJ = Sh::S_STATE / NT;
+    static_assert(NT % CPR == 0 && Sh::S_STATE % NT == 0, "tile split");
     const int r0 = threadIdx.x / CPR, c0 = threadIdx.x % CPR;
     src += (long long)r0 * st_k + c0 * (16 / (int)sizeof(ST));
 #pragma unroll
@@ -77,10 +77,10 @@ __device__ __forceinline__ uint4 *tile_lane_base(uint4 *tile, int kl, int col) {
 
 // Coalesced copy of a tile held in a stage to HBM: dst points at element
 // (row 0, column 0) of the unit's tile, rows st_k elements apart.
-template <typename ST, int K>
+template <typename ST, int K, int NT = PipeShape<ST, K>::NT>
 __device__ __forceinline__ void tile_store(ST *dst, long long st_k, const uint4 *tile) {
     using Sh = PipeShape<ST, K>;
-    constexpr int CPR = Sh::CPR, RPI = Sh::NT / CPR, NJ = Sh::S_STATE / Sh::NT;
+    constexpr int CPR = Sh::CPR, RPI = NT / CPR, NJ = Sh::S_STATE / NT;
     const int r0 = threadIdx.x / CPR, c0 = threadIdx.x % CPR;
     dst += (long long)r0 * st_k + c0 * (16 / (int)sizeof(ST));
 #pragma unroll

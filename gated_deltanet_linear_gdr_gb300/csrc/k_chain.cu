@@ -49,10 +49,11 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
     constexpr int WC = Sh::WC, W = Sh::W, NT = Sh::NT, VS = Sh::VS, SLICES = Sh::SLICES;
     constexpr int KP = Sh::KP, TC = Sh::TC;
 
-    __shared__ __align__(16) float q_s[TC][KP];
-    __shared__ __align__(16) float k_s[TC][KP];
-    __shared__ __align__(16) float v_s[TC][VS];
-    __shared__ __align__(16) float sc_s[TC][4];  // alpha, beta, k^.q~
+    // two chunk buffers: chunk i+1 is copied in while chunk i is processed
+    __shared__ __align__(16) float q_s[2][TC][KP];
+    __shared__ __align__(16) float k_s[2][TC][KP];
+    __shared__ __align__(16) float v_s[2][TC][VS];
+    __shared__ __align__(16) float sc_s[2][TC][4];  // decay -> alpha, beta, k^.q~
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kl = lane % LK, vl = lane / LK;
@@ -122,34 +123,71 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
     const long long voff = (long long)(2 * p.nk * K + h * V + slice * VS) * p.qkv_cs;
     bool overflow = false;
 
-    for (int cb = 0; cb < L; cb += TC) {
-        const int tc = min(TC, L - cb);
-        __syncthreads();  // previous chunk fully consumed
-        // ---- stage raw operands of tc tokens
-        for (int idx = tid; idx < tc * K; idx += NT) {
-            const int tt = idx / K, i = idx - tt * K;
-            const float *row = p.qkv + (long long)(t0 + cb + tt) * p.qkv_ss;
-            q_s[tt][pidx<ROWS>(i)] = row[qoff + (long long)i * p.qkv_cs];
-            k_s[tt][pidx<ROWS>(i)] = row[koff + (long long)i * p.qkv_cs];
+    // Raw operands of tokens [cb, cb + tc) into buffer bi; one cp.async group.
+    auto stage = [&](int cb, int tc, int bi) {
+        if (p.qkv_vec) {
+            constexpr int RQ = K / 4, RVS = VS / 4, RT = 2 * RQ + RVS;
+            for (int idx = tid; idx < tc * RT; idx += NT) {
+                const int tt = idx / RT, r = idx - tt * RT;
+                const float *row = p.qkv + (long long)(t0 + cb + tt) * p.qkv_ss;
+                if (r < RQ)
+                    cp_async16(&q_s[bi][tt][pidx<ROWS>(4 * r)], row + qoff + 4 * r);
+                else if (r < 2 * RQ)
+                    cp_async16(&k_s[bi][tt][pidx<ROWS>(4 * (r - RQ))], row + koff + 4 * (r - RQ));
+                else
+                    cp_async16(&v_s[bi][tt][4 * (r - 2 * RQ)], row + voff + 4 * (r - 2 * RQ));
+            }
+            for (int tt = tid; tt < tc; tt += NT) {
+                const long long o = (long long)(t0 + cb + tt) * p.tok_ss + (long long)h * p.tok_hs;
+                cp_async4(&sc_s[bi][tt][0], p.decay + o);
+                cp_async4(&sc_s[bi][tt][1], p.beta + o);
+            }
+        } else {
+            for (int idx = tid; idx < tc * K; idx += NT) {
+                const int tt = idx / K, i = idx - tt * K;
+                const float *row = p.qkv + (long long)(t0 + cb + tt) * p.qkv_ss;
+                q_s[bi][tt][pidx<ROWS>(i)] = row[qoff + (long long)i * p.qkv_cs];
+                k_s[bi][tt][pidx<ROWS>(i)] = row[koff + (long long)i * p.qkv_cs];
+            }
+            for (int idx = tid; idx < tc * VS; idx += NT) {
+                const int tt = idx / VS, j = idx - tt * VS;
+                v_s[bi][tt][j] = p.qkv[(long long)(t0 + cb + tt) * p.qkv_ss + voff + (long long)j * p.qkv_cs];
+            }
+            for (int tt = tid; tt < tc; tt += NT) {
+                const long long o = (long long)(t0 + cb + tt) * p.tok_ss + (long long)h * p.tok_hs;
+                sc_s[bi][tt][0] = p.decay[o];
+                sc_s[bi][tt][1] = p.beta[o];
+            }
         }
-        for (int idx = tid; idx < tc * VS; idx += NT) {
-            const int tt = idx / VS, j = idx - tt * VS;
-            v_s[tt][j] = p.qkv[(long long)(t0 + cb + tt) * p.qkv_ss + voff + (long long)j * p.qkv_cs];
-        }
-        for (int tt = tid; tt < tc; tt += NT) {
-            const long long o = (long long)(t0 + cb + tt) * p.tok_ss + (long long)h * p.tok_hs;
-            sc_s[tt][0] = gdr_alpha(p.decay[o], p.decay_is_log);
-            sc_s[tt][1] = p.beta[o];
+        cp_async_commit();
+    };
+
+    const int nch = (L + TC - 1) / TC;
+    stage(0, min(TC, L), 0);
+    for (int ci = 0; ci < nch; ++ci) {
+        const int cb = ci * TC, tc = min(TC, L - cb), bi = ci & 1;
+        if (ci + 1 < nch) {
+            stage(cb + TC, min(TC, L - cb - TC), bi ^ 1);  // its buffer was released at the end of ci-1
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
         }
         __syncthreads();
+        float(*qb)[KP] = q_s[bi];
+        float(*kb)[KP] = k_s[bi];
+        float(*vb)[VS] = v_s[bi];
+        float(*sb)[4] = sc_s[bi];
         // ---- normalise: warp w takes tokens w, w+W, ...; lane l works on group l % NG
         for (int tt = warp; tt < tc; tt += W) {
             const int g = lane % NG;
+            const int o = pidx<ROWS>(g * 8);
             float q8[8], k8[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                q8[i] = q_s[tt][pidx<ROWS>(g * 8 + i)];
-                k8[i] = k_s[tt][pidx<ROWS>(g * 8 + i)];
+            for (int i = 0; i < 8; i += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(&qb[tt][o + i]);
+                const float4 b4 = *reinterpret_cast<const float4 *>(&kb[tt][o + i]);
+                q8[i] = a4.x; q8[i + 1] = a4.y; q8[i + 2] = a4.z; q8[i + 3] = a4.w;
+                k8[i] = b4.x; k8[i + 1] = b4.y; k8[i + 2] = b4.z; k8[i + 3] = b4.w;
             }
             float ssq = chain_first(q8[0], q8[0]), ssk = chain_first(k8[0], k8[0]);
             float kqr = chain_first(k8[0], q8[0]);
@@ -164,15 +202,23 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
             kqr = tree_lanes<NG>(kqr);
             float inv_k, qsc, kq;
             gdr_norm_scalars(ssq, ssk, kqr, p.l2norm, p.scale, p.eps, inv_k, qsc, kq);
+            const float alpha = gdr_alpha(sb[tt][0], p.decay_is_log);
             __syncwarp();
             if (lane < NG) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    k_s[tt][pidx<ROWS>(g * 8 + i)] = __fmul_rn(k8[i], inv_k);
-                    q_s[tt][pidx<ROWS>(g * 8 + i)] = __fmul_rn(q8[i], qsc);
+                for (int i = 0; i < 8; i += 4) {
+                    *reinterpret_cast<float4 *>(&kb[tt][o + i]) =
+                        make_float4(__fmul_rn(k8[i], inv_k), __fmul_rn(k8[i + 1], inv_k),
+                                    __fmul_rn(k8[i + 2], inv_k), __fmul_rn(k8[i + 3], inv_k));
+                    *reinterpret_cast<float4 *>(&qb[tt][o + i]) =
+                        make_float4(__fmul_rn(q8[i], qsc), __fmul_rn(q8[i + 1], qsc),
+                                    __fmul_rn(q8[i + 2], qsc), __fmul_rn(q8[i + 3], qsc));
                 }
             }
-            if (lane == 0) sc_s[tt][2] = kq;
+            if (lane == 0) {
+                sb[tt][0] = alpha;
+                sb[tt][2] = kq;
+            }
         }
         __syncthreads();
 
@@ -183,8 +229,8 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
         for (int g = 0; g < RG; ++g) {
 #pragma unroll
             for (int i4 = 0; i4 < 2; ++i4) {
-                const float4 kn = *reinterpret_cast<const float4 *>(&k_s[0][rb + g * 8 + i4 * 4]);
-                const float4 qn = *reinterpret_cast<const float4 *>(&q_s[0][rb + g * 8 + i4 * 4]);
+                const float4 kn = *reinterpret_cast<const float4 *>(&kb[0][rb + g * 8 + i4 * 4]);
+                const float4 qn = *reinterpret_cast<const float4 *>(&qb[0][rb + g * 8 + i4 * 4]);
                 const float knv[4] = {kn.x, kn.y, kn.z, kn.w}, qnv[4] = {qn.x, qn.y, qn.z, qn.w};
 #pragma unroll
                 for (int ii = 0; ii < 4; ++ii) {
@@ -202,7 +248,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
 
         // ---- the chunk's tokens
         for (int tt = 0; tt < tc; ++tt) {
-            const float alpha = sc_s[tt][0], beta = sc_s[tt][1], kq = sc_s[tt][2];
+            const float alpha = sb[tt][0], beta = sb[tt][1], kq = sb[tt][2];
             float u[C], o[C];
 #pragma unroll
             for (int c = 0; c < C; ++c) {
@@ -214,7 +260,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
                 }
                 const float A = tree_lanes<LK>(tree<RG>(ac));
                 const float B = tree_lanes<LK>(tree<RG>(bc));
-                u[c] = gdr_u(beta, alpha, A, v_s[tt][wcol + c]);
+                u[c] = gdr_u(beta, alpha, A, vb[tt][wcol + c]);
                 o[c] = gdr_o(alpha, B, kq, u[c]);
             }
             const int step = cb + tt;  // token index inside the row
@@ -229,7 +275,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
                     if (slice == 0) {
                         if (tid == 0) rec[rp.alpha_off + jr] = alpha;
                         if (jr == 0)
-                            for (int i = tid; i < K; i += NT) rec[i] = k_s[tt][pidx<ROWS>(i)];
+                            for (int i = tid; i < K; i += NT) rec[i] = kb[tt][pidx<ROWS>(i)];
                     }
                 }
             }
@@ -240,12 +286,12 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
 #pragma unroll
                 for (int i4 = 0; i4 < 2; ++i4) {
                     const int o4 = rb + g * 8 + i4 * 4;
-                    const float4 kc = *reinterpret_cast<const float4 *>(&k_s[tt][o4]);
+                    const float4 kc = *reinterpret_cast<const float4 *>(&kb[tt][o4]);
                     const float kcv[4] = {kc.x, kc.y, kc.z, kc.w};
                     float knv[4] = {0.f, 0.f, 0.f, 0.f}, qnv[4] = {0.f, 0.f, 0.f, 0.f};
                     if (next) {
-                        const float4 kn = *reinterpret_cast<const float4 *>(&k_s[tt + 1][o4]);
-                        const float4 qn = *reinterpret_cast<const float4 *>(&q_s[tt + 1][o4]);
+                        const float4 kn = *reinterpret_cast<const float4 *>(&kb[tt + 1][o4]);
+                        const float4 qn = *reinterpret_cast<const float4 *>(&qb[tt + 1][o4]);
                         knv[0] = kn.x; knv[1] = kn.y; knv[2] = kn.z; knv[3] = kn.w;
                         qnv[0] = qn.x; qnv[1] = qn.y; qnv[2] = qn.z; qnv[3] = qn.w;
                     }
@@ -283,6 +329,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
                 }
             }
         }
+        __syncthreads();  // every warp is done with buffer bi before chunk ci+2 is copied into it
     }
     if constexpr (MODE == Mode::Snap) {
         if (overflow && leader) flag(p.status, GDR_STATUS_SNAPSHOT_OVERFLOW);

@@ -16,7 +16,6 @@
 namespace gdr {
 
 constexpr int kFoldThreads = 256;
-constexpr int kMaxRingLen = 32;
 
 template <typename ST, int K> struct FoldShape {
     static constexpr int V = K;

@@ -7,26 +7,48 @@
 // pipelined decode kernel.  A unit's stage holds the bf16/f32 state tile and
 // the operands of its first TCH tokens, all copied with cp.async while the
 // previous unit computes.  The tile is widened into float32 registers once
-// (lane = 8 rows x C columns) and stays there for the whole row.  For each
-// staged chunk the CTA's warps first normalise one token each (q~, k^, alpha
-// and k^.q~ written back into the stage), then every warp runs the chunk's
-// tokens on its columns with warp shuffles only.  Snapshots and the final
-// commit go back through the stage and leave the SM as coalesced rows.  Rows
-// longer than TCH load further chunks in place.  The arithmetic is the fixed
-// sequence of gdr_device.cuh, so results equal the other kernels' bit for bit.
+// and stays there for the whole row: lane kl = lane % LK holds RG consecutive
+// 8-row groups, lane vl = lane / LK holds C columns.  With bf16 pools LK = 4
+// (32 rows x 2 columns per lane), so two of a token's tree levels are
+// in-thread adds and the rest is a 4-lane reduce-scatter.  For each staged
+// chunk the CTA's warps first normalise one token each (q~, k^, alpha and
+// k^.q~ written back into the stage), then every warp runs the chunk's tokens
+// on its columns with warp shuffles only.  Snapshots and the final commit go
+// back through the stage and leave the SM as coalesced rows.  Rows longer than
+// TCH load further chunks in place.  The arithmetic is the fixed sequence of
+// gdr_device.cuh, so results equal the other kernels' bit for bit.
 #include "gdr_pipe.cuh"
 
 namespace gdr {
 
-template <typename ST, int K> struct ShortShape {
-    using P = PipeShape<ST, K>;
-    static constexpr int TCH = 8;                        // tokens per staged chunk
-    static constexpr int TQ = K / 4, TK = K / 4, TV = P::CW / 4;
-    static constexpr int TOKV = TQ + TK + TV;            // 16-byte vector chunks per token
+template <typename ST, int K> struct WinShape {
+    using P = PipeShape<ST, K>;                          // tile geometry (CW, CPR, S_STATE, USL)
+    static constexpr bool BF = sizeof(ST) == 2;
+    static constexpr int LK = BF ? cmin(4, K / 8) : P::LK;  // lanes along K
+    static constexpr int RG = K / 8 / LK;                // 8-row groups per lane
+    static constexpr int ROWS = 8 * RG;
+    static constexpr int LV = 32 / LK;
+    static constexpr int C = BF ? 2 : P::C;              // columns per lane
+    static constexpr int WC = LV * C;
+    static constexpr int NW = P::CW / WC;                // warps per CTA
+    static constexpr int NT = 32 * NW;
+    static constexpr bool PAD = LK <= 4;                 // pad staged vectors per lane run
+    static constexpr int KP = PAD ? K + LK * 4 : K;      // floats per staged q / k vector
+    static constexpr int TQ = KP / 4, TV = P::CW / 4;    // 16-byte chunks
+    static constexpr int TOKV = 2 * TQ + TV;
     static constexpr int TOK = TOKV + 1;                 // + {decay -> alpha, beta, k^.q~, -}
+    static constexpr int TCH = 8;                        // tokens per staged chunk
     static constexpr int SC = P::S_STATE + TCH * TOK;    // chunks per stage
     static constexpr int SMEM1 = SC * 16;
 };
+
+// Float offset of row i inside a staged q / k vector (4 spare floats after each
+// lane's run of rows keep the LK distinct 16-byte reads in different banks).
+template <typename ST, int K> __device__ __forceinline__ int tpos(int i) {
+    using W = WinShape<ST, K>;
+    if constexpr (W::PAD) return i + (i / W::ROWS) * 4;
+    return i;
+}
 
 // A unit of the short kernel: hu = h * USL + us; b = row.  Past the end of
 // the batch: an empty row.
@@ -58,22 +80,32 @@ __device__ __forceinline__ bool short_unit_valid(const StepParams &p, const Shor
 template <typename ST, int K>
 __device__ __forceinline__ void short_issue_tokens(const StepParams &p, const ShortMeta &m, int cb, int tc,
                                                    uint4 *stage) {
-    using Sh = ShortShape<ST, K>;
+    using W = WinShape<ST, K>;
     using P = PipeShape<ST, K>;
+    constexpr int RQ = K / 4;  // raw chunks per q / k vector
+    constexpr int RV = 2 * RQ + W::TV;
     const int h = m.hu / P::USL, us = m.hu % P::USL;
     const int hk = h / p.r;
     uint4 *tok = stage + P::S_STATE;
-    for (int ch = threadIdx.x; ch < tc * Sh::TOKV; ch += P::NT) {
-        const int tt = ch / Sh::TOKV, r = ch - tt * Sh::TOKV;
+    for (int ch = threadIdx.x; ch < tc * RV; ch += W::NT) {
+        const int tt = ch / RV, r = ch - tt * RV;
         const float *trow = p.qkv + (long long)(m.t0 + cb + tt) * p.qkv_ss;
-        const float *g = r < Sh::TQ ? trow + hk * K + 4 * r
-                         : r < Sh::TQ + Sh::TK ? trow + (p.nk + hk) * K + 4 * (r - Sh::TQ)
-                                               : trow + 2 * p.nk * K + h * K + us * P::CW +
-                                                     4 * (r - Sh::TQ - Sh::TK);
-        cp_async16(tok + tt * Sh::TOK + r, g);
+        const float *g;
+        int dst;
+        if (r < RQ) {
+            g = trow + hk * K + 4 * r;
+            dst = tpos<ST, K>(4 * r) / 4;
+        } else if (r < 2 * RQ) {
+            g = trow + (p.nk + hk) * K + 4 * (r - RQ);
+            dst = W::TQ + tpos<ST, K>(4 * (r - RQ)) / 4;
+        } else {
+            g = trow + 2 * p.nk * K + h * K + us * P::CW + 4 * (r - 2 * RQ);
+            dst = 2 * W::TQ + (r - 2 * RQ);
+        }
+        cp_async16(tok + tt * W::TOK + dst, g);
     }
-    for (int tt = threadIdx.x; tt < tc; tt += P::NT) {
-        float *ab = reinterpret_cast<float *>(tok + tt * Sh::TOK + Sh::TOKV);
+    for (int tt = threadIdx.x; tt < tc; tt += W::NT) {
+        float *ab = reinterpret_cast<float *>(tok + tt * W::TOK + W::TOKV);
         const long long o = (long long)(m.t0 + cb + tt) * p.tok_ss + (long long)h * p.tok_hs;
         cp_async4(ab, p.decay + o);
         cp_async4(ab + 1, p.beta + o);
@@ -84,24 +116,38 @@ template <typename ST, int K>
 __device__ __forceinline__ void short_issue(const StepParams &p, const ShortMeta &m, long long max_len,
                                             uint4 *stage) {
     using P = PipeShape<ST, K>;
-    constexpr int TCH = ShortShape<ST, K>::TCH;
+    using W = WinShape<ST, K>;
     if (short_unit_valid(p, m, max_len)) {
         const int h = m.hu / P::USL, us = m.hu % P::USL;
-        tile_issue<ST, K>(reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
-                              (long long)h * p.st_head + us * P::CW,
-                          p.st_k, stage);
+        tile_issue<ST, K, W::NT>(reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
+                                     (long long)h * p.st_head + us * P::CW,
+                                 p.st_k, stage);
         const int L = m.t1 - m.t0;
-        short_issue_tokens<ST, K>(p, m, 0, L < TCH ? L : TCH, stage);
+        short_issue_tokens<ST, K>(p, m, 0, L < W::TCH ? L : W::TCH, stage);
     }
     cp_async_commit();
 }
 
-// Writes the float32 state s (this lane's 8 rows x C columns) into the tile.
+// This lane's C columns of tile row r (rows keep the 16-byte chunk swizzle).
 template <typename ST, int K>
-__device__ __forceinline__ void short_put_tile(uint4 *mine, const float (&s)[8][PipeShape<ST, K>::C]) {
-    constexpr int C = PipeShape<ST, K>::C, CPR = PipeShape<ST, K>::CPR;
+__device__ __forceinline__ ST *tile_cols(uint4 *tile, int r, int col) {
+    using P = PipeShape<ST, K>;
+    constexpr int EPC = 16 / (int)sizeof(ST);
+    return reinterpret_cast<ST *>(tile + r * P::CPR + ((col / EPC) ^ ((r >> 3) & (P::CPR - 1)))) + (col % EPC);
+}
+
+// Writes the float32 state s (this lane's ROWS rows x C columns) into the tile.
+template <typename ST, int K>
+__device__ __forceinline__ void short_put_tile(uint4 *tile, int r0, int col,
+                                               const float (&s)[WinShape<ST, K>::ROWS][WinShape<ST, K>::C]) {
+    constexpr int ROWS = WinShape<ST, K>::ROWS, C = WinShape<ST, K>::C;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) pack_store<ST, C>(mine + i * CPR, s[i]);
+    for (int i = 0; i < ROWS; ++i) {
+        Pack<ST, C> x;
+#pragma unroll
+        for (int c = 0; c < C; ++c) x.set(c, s[i][c]);
+        x.store(tile_cols<ST, K>(tile, r0 + i, col));
+    }
 }
 
 // Computes one unit; returns true when the state must be committed (the new
@@ -111,9 +157,13 @@ template <typename ST, int K, Mode MODE>
 __device__ __forceinline__ bool short_compute(const StepParams &p, const RingParams &rp, const SnapParams &sp,
                                               long long max_len, const ShortMeta &m, uint4 *stage) {
     using P = PipeShape<ST, K>;
-    using Sh = ShortShape<ST, K>;
-    constexpr int V = K, NG = K / 8, LK = P::LK, C = P::C, CPR = P::CPR, NW = P::NW, TCH = Sh::TCH;
-    using VT = typename Pack<ST, C>::VT;
+    using W = WinShape<ST, K>;
+    constexpr int V = K, NG = K / 8, LK = W::LK, RG = W::RG, ROWS = W::ROWS, C = W::C, NW = W::NW;
+    constexpr int TCH = W::TCH;
+    // Across few lanes a butterfly (every lane ends with every sum, two shuffle
+    // rounds for LK = 4) has a shorter critical path than reduce-scatter +
+    // broadcast; both follow the same tree.
+    constexpr bool kUseRS = LK == 2 * C && LK > 4;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kl = lane % LK, vl = lane / LK;
     const int h = m.hu / P::USL, us = m.hu % P::USL;
@@ -129,7 +179,7 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
         if (leader) flag(p.status, GDR_STATUS_ROW_TOO_LONG);
         return false;
     }
-    const int col = warp * P::WC + vl * C;  // inside the unit's tile
+    const int col = warp * W::WC + vl * C;  // inside the unit's tile
     float *obase = p.out + (long long)m.t0 * p.out_ss + (long long)(h * V + us * P::CW + col) * p.out_vs;
     if (m.slot < 0 || m.slot >= p.max_slots) {
         if (m.slot != -1 && leader) flag(p.status, GDR_STATUS_BAD_SLOT);
@@ -157,17 +207,31 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
         }
     }
 
-    uint4 *mine = tile_lane_base<ST, K>(stage, kl, col);
-    float s[8][C];
+    const int r0 = kl * ROWS;  // this lane's first tile row
+    float s[ROWS][C];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < ROWS; ++i) {
         Pack<ST, C> x;
-        x.u.v = *reinterpret_cast<const VT *>(mine + i * CPR);
+        x.load(tile_cols<ST, K>(stage, r0 + i, col));
 #pragma unroll
         for (int c = 0; c < C; ++c) s[i][c] = x.get(c);
     }
     float *tokf = reinterpret_cast<float *>(stage + P::S_STATE);
     bool overflow = false;
+    // Per-lane output and record pointers, advanced by one token per step.
+    // With the reduce-scatter the lane pair (kl, kl^1) owns column ocol; the
+    // even lane writes it.  Otherwise lanes kl == 0 write all C columns.
+    int ocol = col;
+    bool w_out = kl == 0;
+    if constexpr (kUseRS) {
+        ocol = col + rs_column<LK, C>(kl);
+        w_out = !(kl & 1);
+    }
+    float *optr = p.out + (long long)m.t0 * p.out_ss + (long long)(h * V + us * P::CW + ocol) * p.out_vs;
+    float *uptr0 = ring_row;  // record of the current token
+    float *uptr = records ? ring_row + rp.u_off + jr * V + us * P::CW + ocol : nullptr;
+    const bool w_alpha = records && us == 0 && tid == 0;
+    const bool w_kh = records && us == 0 && jr == 0 && warp == 0 && vl == 0;
 
     for (int cb = 0; cb < L; cb += TCH) {
         const int tc = min(TCH, L - cb);
@@ -180,15 +244,16 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
         }
         // normalise: warp w takes tokens w, w+NW, ...; lane l works on row group l % NG
         for (int tt = warp; tt < tc; tt += NW) {
-            float *tq = tokf + tt * Sh::TOK * 4;
-            float *tk = tq + K;
-            float *ab = tq + Sh::TOKV * 4;
+            float *tq = tokf + tt * W::TOK * 4;
+            float *tk = tq + W::KP;
+            float *ab = tq + W::TOKV * 4;
             const int g = lane % NG;
+            const int o = tpos<ST, K>(g * 8);
             float q8[8], k8[8];
 #pragma unroll
             for (int i = 0; i < 8; i += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(tq + g * 8 + i);
-                const float4 b4 = *reinterpret_cast<const float4 *>(tk + g * 8 + i);
+                const float4 a4 = *reinterpret_cast<const float4 *>(tq + o + i);
+                const float4 b4 = *reinterpret_cast<const float4 *>(tk + o + i);
                 q8[i] = a4.x; q8[i + 1] = a4.y; q8[i + 2] = a4.z; q8[i + 3] = a4.w;
                 k8[i] = b4.x; k8[i + 1] = b4.y; k8[i + 2] = b4.z; k8[i + 3] = b4.w;
             }
@@ -210,10 +275,10 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
             if (lane < NG) {
 #pragma unroll
                 for (int i = 0; i < 8; i += 4) {
-                    *reinterpret_cast<float4 *>(tk + g * 8 + i) =
+                    *reinterpret_cast<float4 *>(tk + o + i) =
                         make_float4(__fmul_rn(k8[i], inv_k), __fmul_rn(k8[i + 1], inv_k),
                                     __fmul_rn(k8[i + 2], inv_k), __fmul_rn(k8[i + 3], inv_k));
-                    *reinterpret_cast<float4 *>(tq + g * 8 + i) =
+                    *reinterpret_cast<float4 *>(tq + o + i) =
                         make_float4(__fmul_rn(q8[i], qsc), __fmul_rn(q8[i + 1], qsc),
                                     __fmul_rn(q8[i + 2], qsc), __fmul_rn(q8[i + 3], qsc));
                 }
@@ -225,40 +290,53 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
         }
         __syncthreads();
 
-        for (int tt = 0; tt < tc; ++tt) {
-            const float *tq = tokf + tt * Sh::TOK * 4;
-            const float *tk = tq + K;
-            const float *tv = tk + K;
-            const float *ab = tq + Sh::TOKV * 4;
+        const float *tq = tokf;  // operands of token cb + tt, advanced per token
+        for (int tt = 0; tt < tc; ++tt, tq += W::TOK * 4) {
+            const float *tk = tq + W::KP;
+            const float *ab = tq + W::TOKV * 4;
             const float alpha = ab[0], beta = ab[1], kq = ab[2];
-            float kh[8], qt[8];
+            const int base = tpos<ST, K>(r0);  // this lane's run of rows in the staged vectors
+            // a = S^T k^, b = S^T q~: one chain per 8-row group, then the tree.
+            float pa[RG][C], pb[RG][C];
 #pragma unroll
-            for (int i = 0; i < 8; i += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(tk + kl * 8 + i);
-                const float4 b4 = *reinterpret_cast<const float4 *>(tq + kl * 8 + i);
-                kh[i] = a4.x; kh[i + 1] = a4.y; kh[i + 2] = a4.z; kh[i + 3] = a4.w;
-                qt[i] = b4.x; qt[i + 1] = b4.y; qt[i + 2] = b4.z; qt[i + 3] = b4.w;
+            for (int g = 0; g < RG; ++g) {
+                float kh[8], qt[8];
+#pragma unroll
+                for (int i = 0; i < 8; i += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(tk + base + g * 8 + i);
+                    const float4 b4 = *reinterpret_cast<const float4 *>(tq + base + g * 8 + i);
+                    kh[i] = a4.x; kh[i + 1] = a4.y; kh[i + 2] = a4.z; kh[i + 3] = a4.w;
+                    qt[i] = b4.x; qt[i + 1] = b4.y; qt[i + 2] = b4.z; qt[i + 3] = b4.w;
+                }
+                chain_first_cols<C>(s[g * 8], kh[0], pa[g]);
+                chain_first_cols<C>(s[g * 8], qt[0], pb[g]);
+#pragma unroll
+                for (int i = 1; i < 8; ++i) {
+                    chain_next_cols<C>(s[g * 8 + i], kh[i], pa[g]);
+                    chain_next_cols<C>(s[g * 8 + i], qt[i], pb[g]);
+                }
             }
             float a[C], bq[C];
-            chain_first_cols<C>(s[0], kh[0], a);
-            chain_first_cols<C>(s[0], qt[0], bq);
 #pragma unroll
-            for (int i = 1; i < 8; ++i) {
-                chain_next_cols<C>(s[i], kh[i], a);
-                chain_next_cols<C>(s[i], qt[i], bq);
+            for (int c = 0; c < C; ++c) {
+                float ac[RG], bc[RG];
+#pragma unroll
+                for (int g = 0; g < RG; ++g) {
+                    ac[g] = pa[g][c];
+                    bc[g] = pb[g][c];
+                }
+                a[c] = tree<RG>(ac);
+                bq[c] = tree<RG>(bc);
             }
-            const int step = cb + tt;  // token index inside the row
-            float *orow = obase + (long long)step * p.out_ss;
-            float *rec = records ? ring_row + (long long)step * rp.stride : nullptr;
+            const float *tv = tq + 2 * W::KP;
             float u[C];
-            if constexpr (LK == 2 * C) {
+            if constexpr (kUseRS) {
                 float A, B;
                 rs_reduce<LK, C>(a, bq, kl, A, B);
-                const int c = rs_column<LK, C>(kl);
-                const float uc = gdr_u(beta, alpha, A, tv[col + c]);
-                if (!(kl & 1)) {
-                    orow[(long long)c * p.out_vs] = gdr_o(alpha, B, kq, uc);
-                    if (records) rec[rp.u_off + jr * V + us * P::CW + col + c] = uc;
+                const float uc = gdr_u(beta, alpha, A, tv[ocol]);
+                if (w_out) {
+                    *optr = gdr_o(alpha, B, kq, uc);
+                    if (records) *uptr = uc;
                 }
                 rs_broadcast<LK, C>(uc, lane, u);
             } else {
@@ -269,32 +347,48 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
                     u[c] = gdr_u(beta, alpha, A, tv[col + c]);
                     a[c] = gdr_o(alpha, B, kq, u[c]);  // the output
                 }
-                if (kl == 0) {
-                    store_f32<C>(orow, p.out_vs, p.out_vec, a);
+                if (w_out) {
+                    store_f32<C>(optr, p.out_vs, p.out_vec, a);
                     if (records) {
 #pragma unroll
-                        for (int c = 0; c < C; ++c) rec[rp.u_off + jr * V + us * P::CW + col + c] = u[c];
+                        for (int c = 0; c < C; ++c) uptr[c] = u[c];
                     }
                 }
             }
-            if (records && us == 0) {
-                if (tid == 0) rec[rp.alpha_off + jr] = alpha;
-                if (jr == 0 && warp == 0 && vl == 0) {
-                    *reinterpret_cast<float4 *>(rec + kl * 8) = make_float4(kh[0], kh[1], kh[2], kh[3]);
-                    *reinterpret_cast<float4 *>(rec + kl * 8 + 4) = make_float4(kh[4], kh[5], kh[6], kh[7]);
-                }
-            }
+            if (w_alpha) uptr0[rp.alpha_off + jr] = alpha;
+            if (w_kh) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) advance_cols<C>(s[i], kh[i], u, alpha);
+                for (int i = 0; i < ROWS; i += 4)
+                    *reinterpret_cast<float4 *>(uptr0 + r0 + i) = *reinterpret_cast<const float4 *>(tk + base + i);
+            }
+            optr += p.out_ss;
+            if (records) {
+                uptr += rp.stride;
+                uptr0 += rp.stride;
+            }
+            // S <- k^ u^T + alpha S
+#pragma unroll
+            for (int g = 0; g < RG; ++g) {
+                float kh[8];
+#pragma unroll
+                for (int i = 0; i < 8; i += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(tk + base + g * 8 + i);
+                    kh[i] = a4.x; kh[i + 1] = a4.y; kh[i + 2] = a4.z; kh[i + 3] = a4.w;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) advance_cols<C>(s[g * 8 + i], kh[i], u, alpha);
+            }
+            const int step = cb + tt;  // token index inside the row
             if constexpr (MODE == Mode::Snap) {
                 if ((step + 1) % sp.spt == 0) {
                     const int i = (step + 1) / sp.spt - 1;
                     if (i < sp.n_inter) {
-                        short_put_tile<ST, K>(mine, s);
+                        short_put_tile<ST, K>(stage, r0, col, s);
                         __syncthreads();
-                        tile_store<ST, K>(reinterpret_cast<ST *>(sp.inter) + (long long)m.slot * sp.s_slot +
-                                              (long long)i * sp.s_tok + (long long)h * sp.s_head + us * P::CW,
-                                          V, stage);
+                        tile_store<ST, K, W::NT>(reinterpret_cast<ST *>(sp.inter) + (long long)m.slot * sp.s_slot +
+                                                     (long long)i * sp.s_tok + (long long)h * sp.s_head +
+                                                     us * P::CW,
+                                                 V, stage);
                         __syncthreads();
                     } else {
                         overflow = true;
@@ -306,18 +400,18 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
     if constexpr (MODE == Mode::Snap) {
         if (overflow && leader) flag(p.status, GDR_STATUS_SNAPSHOT_OVERFLOW);
     }
-    if (commit) short_put_tile<ST, K>(mine, s);
+    if (commit) short_put_tile<ST, K>(stage, r0, col, s);
     return commit;
 }
 
 template <typename ST, int K, Mode MODE>
-__global__ void __launch_bounds__(PipeShape<ST, K>::NT, 2)
+__global__ void __launch_bounds__(WinShape<ST, K>::NT, 2)
     k_short(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len,
             const int nunits) {
     using P = PipeShape<ST, K>;
-    using Sh = ShortShape<ST, K>;
+    using W = WinShape<ST, K>;
     extern __shared__ uint4 smem_short[];
-    uint4 *stage0 = smem_short, *stage1 = smem_short + Sh::SC;
+    uint4 *stage0 = smem_short, *stage1 = smem_short + W::SC;
     const long long G = gridDim.x;
     ShortMeta cur = short_meta<P::USL>(p, blockIdx.x, nunits);
     short_issue<ST, K>(p, cur, max_len, stage0);
@@ -334,9 +428,9 @@ __global__ void __launch_bounds__(PipeShape<ST, K>::NT, 2)
         __syncthreads();
         if (commit) {
             const int h = cur.hu / P::USL, us = cur.hu % P::USL;
-            tile_store<ST, K>(reinterpret_cast<ST *>(p.state) + (long long)cur.slot * p.st_slot +
-                                  (long long)h * p.st_head + us * P::CW,
-                              p.st_k, s_cur);
+            tile_store<ST, K, W::NT>(reinterpret_cast<ST *>(p.state) + (long long)cur.slot * p.st_slot +
+                                         (long long)h * p.st_head + us * P::CW,
+                                     p.st_k, s_cur);
         }
         __syncthreads();
         cur = nxt;
@@ -350,7 +444,8 @@ template <typename ST, int K, Mode MODE>
 static cudaError_t launch_short_m(const StepParams &p, const RingParams &rp, const SnapParams &sp,
                                   long long max_len, cudaStream_t st) {
     using P = PipeShape<ST, K>;
-    constexpr int SMEM = 2 * ShortShape<ST, K>::SMEM1;
+    using W = WinShape<ST, K>;
+    constexpr int SMEM = 2 * W::SMEM1;
     static int configured[64] = {0};
     static int sms[64] = {0}, occ[64] = {0};
     int dev = 0;
@@ -362,7 +457,7 @@ static cudaError_t launch_short_m(const StepParams &p, const RingParams &rp, con
         if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[dev], k_short<ST, K, MODE>, P::NT, SMEM);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[dev], k_short<ST, K, MODE>, W::NT, SMEM);
         if (e != cudaSuccess) return e;
         if (occ[dev] < 1) occ[dev] = 1;
         configured[dev] = 1;
@@ -370,32 +465,30 @@ static cudaError_t launch_short_m(const StepParams &p, const RingParams &rp, con
     const long long nunits = (long long)p.batch * p.nv * P::USL;
     long long grid = (long long)sms[dev] * occ[dev];
     if (grid > nunits) grid = nunits;
-    if (grid > 0) k_short<ST, K, MODE><<<(unsigned)grid, P::NT, SMEM, st>>>(p, rp, sp, max_len, (int)nunits);
+    if (grid > 0) k_short<ST, K, MODE><<<(unsigned)grid, W::NT, SMEM, st>>>(p, rp, sp, max_len, (int)nunits);
     return cudaGetLastError();
 }
 
-template <typename ST, int K>
-static bool short_ok(const StepParams &p) {
-    if constexpr (!PipeShape<ST, K>::OK) {
-        return false;
-    } else {
-        return p.qkv_vec && (long long)p.batch * p.nv * PipeShape<ST, K>::USL < (1ll << 31);
-    }
-}
+template <typename ST, int K> struct ShortOK {
+    static constexpr bool value = PipeShape<ST, K>::OK && WinShape<ST, K>::NT % PipeShape<ST, K>::CPR == 0 &&
+                                  PipeShape<ST, K>::S_STATE % WinShape<ST, K>::NT == 0 &&
+                                  WinShape<ST, K>::NW >= 1;
+};
 
 template <typename ST, int K>
 static cudaError_t launch_short_t(const StepParams &p, Mode mode, const RingParams &rp, const SnapParams &sp,
                                   long long max_len, cudaStream_t st, bool *used) {
-    *used = short_ok<ST, K>(p);
-    if (!*used) return cudaSuccess;
-    if constexpr (PipeShape<ST, K>::OK) {
+    *used = false;
+    if constexpr (ShortOK<ST, K>::value) {
+        if (!p.qkv_vec || (long long)p.batch * p.nv * PipeShape<ST, K>::USL >= (1ll << 31)) return cudaSuccess;
+        *used = true;
         switch (mode) {
             case Mode::Fwd: return launch_short_m<ST, K, Mode::Fwd>(p, rp, sp, max_len, st);
             case Mode::Verify: return launch_short_m<ST, K, Mode::Verify>(p, rp, sp, max_len, st);
             case Mode::Snap: return launch_short_m<ST, K, Mode::Snap>(p, rp, sp, max_len, st);
         }
     }
-    return cudaErrorInvalidValue;
+    return cudaSuccess;
 }
 
 cudaError_t launch_short(const StepParams &p, int K, bool bf16, Mode mode, const RingParams &rp,

@@ -11,14 +11,14 @@
 
 namespace gdr {
 
-template <typename ST, int K> struct PipeShape {
+template <typename ST, int K, int NWMAX = 8> struct PipeShape {
     static constexpr int V = K;
     static constexpr int LK = K / 8;
     static constexpr int LV = 32 / LK;
     static constexpr int C = 16 / (int)sizeof(ST);          // one 16-byte vector per row
     static constexpr bool OK = C <= V / LV;
     static constexpr int WC = LV * C;                       // columns per warp
-    static constexpr int NW = OK ? cmin(8, V / WC) : 1;      // warps per CTA
+    static constexpr int NW = OK ? cmin(NWMAX, V / WC) : 1;  // warps per CTA
     static constexpr int NT = 32 * NW;
     static constexpr int CW = NW * WC;                      // columns per unit
     static constexpr int USL = V / CW;                      // units per (row, head)
@@ -53,9 +53,9 @@ __device__ __forceinline__ UnitMeta unit_meta(const StepParams &p, int u, int nu
 // src, rows st_k elements apart) into shared memory, swizzled.  Every thread
 // of the CTA takes S_STATE / NT chunks; consecutive threads read consecutive
 // 16-byte chunks of a row.
-template <typename ST, int K, int NT = PipeShape<ST, K>::NT>
+template <typename ST, int K, int NT = PipeShape<ST, K>::NT, int NWMAX = 8>
 __device__ __forceinline__ void tile_issue(const ST *src, long long st_k, uint4 *tile) {
-    using Sh = PipeShape<ST, K>;
+    using Sh = PipeShape<ST, K, NWMAX>;
     constexpr int CPR = Sh::CPR, RPI = NT / CPR, NJ = Sh::S_STATE / NT;
     static_assert(NT % CPR == 0 && Sh::S_STATE % NT == 0, "tile split");
     const int r0 = threadIdx.x / CPR, c0 = threadIdx.x % CPR;
@@ -69,17 +69,17 @@ __device__ __forceinline__ void tile_issue(const ST *src, long long st_k, uint4 
 
 // This lane's chunk of tile row 8*kl + i: rows of one 8-row group share the
 // swizzle (row / 8 == kl), so it is a fixed base plus i * CPR.
-template <typename ST, int K>
+template <typename ST, int K, int NWMAX = 8>
 __device__ __forceinline__ uint4 *tile_lane_base(uint4 *tile, int kl, int col) {
-    using Sh = PipeShape<ST, K>;
+    using Sh = PipeShape<ST, K, NWMAX>;
     return tile + kl * 8 * Sh::CPR + ((col / Sh::C) ^ (kl & (Sh::CPR - 1)));
 }
 
 // Coalesced copy of a tile held in a stage to HBM: dst points at element
 // (row 0, column 0) of the unit's tile, rows st_k elements apart.
-template <typename ST, int K, int NT = PipeShape<ST, K>::NT>
+template <typename ST, int K, int NT = PipeShape<ST, K>::NT, int NWMAX = 8>
 __device__ __forceinline__ void tile_store(ST *dst, long long st_k, const uint4 *tile) {
-    using Sh = PipeShape<ST, K>;
+    using Sh = PipeShape<ST, K, NWMAX>;
     constexpr int CPR = Sh::CPR, RPI = NT / CPR, NJ = Sh::S_STATE / NT;
     const int r0 = threadIdx.x / CPR, c0 = threadIdx.x % CPR;
     dst += (long long)r0 * st_k + c0 * (16 / (int)sizeof(ST));

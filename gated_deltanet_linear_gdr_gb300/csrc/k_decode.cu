@@ -137,6 +137,11 @@ __global__ void __launch_bounds__(kDecodeThreads) k_decode(const StepParams p) {
     }
 }
 
+// Warps per CTA (each owns 16 bf16 / 8 f32 columns of a tile) and the
+// pipeline's depth and residency.
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeMinBlocks = 4;
+
 // ---------------------------------------------------------------------------
 // Pipelined variant for the common layouts (16-byte state vectors, unit-stride
 // Q/K/V rows).  Persistent CTAs walk (row, value head, tile) units with a
@@ -150,11 +155,11 @@ __device__ __forceinline__ bool decode_unit_streams(const StepParams &p, const U
 // Queue the copies of one unit into a stage (always commits one group).
 template <typename ST, int K>
 __device__ __forceinline__ void unit_issue(const StepParams &p, const UnitMeta &m, uint4 *stage) {
-    using Sh = PipeShape<ST, K>;
+    using Sh = PipeShape<ST, K, kDecodeWarps>;
     if (decode_unit_streams(p, m)) {
         const int tid = threadIdx.x;
         const int h = m.hu / Sh::USL, us = m.hu % Sh::USL;
-        tile_issue<ST, K>(reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
+        tile_issue<ST, K, PipeShape<ST, K, kDecodeWarps>::NT, kDecodeWarps>(reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
                               (long long)h * p.st_head + us * Sh::CW,
                           p.st_k, stage);
         const int hk = h / p.r;
@@ -178,7 +183,7 @@ __device__ __forceinline__ void unit_issue(const StepParams &p, const UnitMeta &
 
 template <typename ST, int K>
 __device__ __forceinline__ void unit_compute(const StepParams &p, const UnitMeta &m, uint4 *stage) {
-    using Sh = PipeShape<ST, K>;
+    using Sh = PipeShape<ST, K, kDecodeWarps>;
     constexpr int V = K, LK = Sh::LK, C = Sh::C, CPR = Sh::CPR;
     using VT = typename Pack<ST, C>::VT;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -235,7 +240,7 @@ __device__ __forceinline__ void unit_compute(const StepParams &p, const UnitMeta
         k[i] = __fmul_rn(k[i], inv_k);  // k^
         q[i] = __fmul_rn(q[i], qsc);    // q~
     }
-    uint4 *mine = tile_lane_base<ST, K>(stage, kl, col);
+    uint4 *mine = tile_lane_base<ST, K, kDecodeWarps>(stage, kl, col);
     float a[C], bq[C];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -287,9 +292,9 @@ __device__ __forceinline__ void unit_compute(const StepParams &p, const UnitMeta
 }
 
 template <typename ST, int K, int NS>
-__global__ void __launch_bounds__(PipeShape<ST, K>::NT, NS == 2 ? 3 : 2)
+__global__ void __launch_bounds__(PipeShape<ST, K, kDecodeWarps>::NT, kDecodeMinBlocks)
     k_decode_pipe(const StepParams p, const int nunits) {
-    using Sh = PipeShape<ST, K>;
+    using Sh = PipeShape<ST, K, kDecodeWarps>;
     extern __shared__ uint4 smem_pipe[];
     const int G = gridDim.x;
     // mq[s] holds units i .. i+NS-1 (i = this CTA's current unit)
@@ -314,7 +319,7 @@ __global__ void __launch_bounds__(PipeShape<ST, K>::NT, NS == 2 ? 3 : 2)
         __syncthreads();
         if (decode_unit_streams(p, mq[0])) {
             const int h = mq[0].hu / Sh::USL, us = mq[0].hu % Sh::USL;
-            tile_store<ST, K>(reinterpret_cast<ST *>(p.state) + (long long)mq[0].slot * p.st_slot +
+            tile_store<ST, K, PipeShape<ST, K, kDecodeWarps>::NT, kDecodeWarps>(reinterpret_cast<ST *>(p.state) + (long long)mq[0].slot * p.st_slot +
                                   (long long)h * p.st_head + us * Sh::CW,
                               p.st_k, stage);
         }
@@ -329,9 +334,10 @@ __global__ void __launch_bounds__(PipeShape<ST, K>::NT, NS == 2 ? 3 : 2)
 
 // Pipeline depth of the decode kernel (shared-memory stages per CTA).
 constexpr int kDecodeStages = 3;
+static_assert(kDecodeWarps >= 1, "decode CTA");
 
 template <typename ST, int K> static cudaError_t launch_pipe_t(const StepParams &p, cudaStream_t st) {
-    using Sh = PipeShape<ST, K>;
+    using Sh = PipeShape<ST, K, kDecodeWarps>;
     constexpr int NS = kDecodeStages;
     constexpr int SMEM = NS * Sh::SMEM1;
     static int configured[64] = {0};
@@ -365,9 +371,9 @@ template <typename ST, int K> static cudaError_t launch_decode_t(const StepParam
 }
 
 template <typename ST, int K> static cudaError_t launch_decode_any(const StepParams &p, cudaStream_t s) {
-    if constexpr (PipeShape<ST, K>::OK) {
+    if constexpr (PipeShape<ST, K, kDecodeWarps>::OK) {
         // the pipelined kernel counts units in 32 bits
-        if (p.qkv_vec && (long long)p.batch * p.nv * PipeShape<ST, K>::USL < (1ll << 31))
+        if (p.qkv_vec && (long long)p.batch * p.nv * PipeShape<ST, K, kDecodeWarps>::USL < (1ll << 31))
             return launch_pipe_t<ST, K>(p, s);
     }
     return launch_decode_t<ST, K>(p, s);

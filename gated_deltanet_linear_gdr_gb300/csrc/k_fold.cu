@@ -149,6 +149,10 @@ __global__ void __launch_bounds__(kFoldThreads) k_rollback(const RollbackParams 
 // previous unit computes; the new tile leaves through the stage as coalesced
 // rows.  Lane layout and arithmetic as the other pipelined kernels.
 
+// Warps per CTA (tile width) and CTAs per SM of the pipelined fold.
+constexpr int kFoldWarps = 4;
+constexpr int kFoldMinBlocks = 4;
+
 struct FoldMeta {
     int hu, c, slot, rs;  // c == 0: nothing to do
 };
@@ -172,17 +176,17 @@ __device__ __forceinline__ bool fold_active(const FoldParams &p, const FoldMeta 
 }
 
 template <typename ST, int K> struct FoldPipeShape {
-    using P = PipeShape<ST, K>;
+    using P = PipeShape<ST, K, kFoldWarps>;
     static constexpr int RQ = K / 4 + P::CW / 4 + 1;  // 16-byte chunks per staged record
 };
 
 template <typename ST, int K>
 __device__ __forceinline__ void fold_issue(const FoldParams &p, const FoldMeta &m, uint4 *stage) {
-    using P = PipeShape<ST, K>;
+    using P = PipeShape<ST, K, kFoldWarps>;
     using F = FoldPipeShape<ST, K>;
     if (fold_active(p, m)) {
         const int h = m.hu / P::USL, us = m.hu % P::USL;
-        tile_issue<ST, K>(reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
+        tile_issue<ST, K, PipeShape<ST, K, kFoldWarps>::NT, kFoldWarps>(reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
                               (long long)h * p.st_head + us * P::CW,
                           p.st_k, stage);
         const int hk = h / p.r, jr = h % p.r;
@@ -203,7 +207,7 @@ __device__ __forceinline__ void fold_issue(const FoldParams &p, const FoldMeta &
 
 template <typename ST, int K>
 __device__ __forceinline__ bool fold_compute(const FoldParams &p, const FoldMeta &m, uint4 *stage) {
-    using P = PipeShape<ST, K>;
+    using P = PipeShape<ST, K, kFoldWarps>;
     using F = FoldPipeShape<ST, K>;
     constexpr int LK = P::LK, C = P::C, CPR = P::CPR;
     using VT = typename Pack<ST, C>::VT;
@@ -224,7 +228,7 @@ __device__ __forceinline__ bool fold_compute(const FoldParams &p, const FoldMeta
     }
     const int kl = lane % LK, vl = lane / LK;
     const int col = warp * P::WC + vl * C;
-    uint4 *mine = tile_lane_base<ST, K>(stage, kl, col);
+    uint4 *mine = tile_lane_base<ST, K, kFoldWarps>(stage, kl, col);
     float s[8][C];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -257,8 +261,8 @@ __device__ __forceinline__ bool fold_compute(const FoldParams &p, const FoldMeta
 }
 
 template <typename ST, int K>
-__global__ void __launch_bounds__(PipeShape<ST, K>::NT, 2) k_fold_pipe(const FoldParams p, const int nunits) {
-    using P = PipeShape<ST, K>;
+__global__ void __launch_bounds__(PipeShape<ST, K, kFoldWarps>::NT, kFoldMinBlocks) k_fold_pipe(const FoldParams p, const int nunits) {
+    using P = PipeShape<ST, K, kFoldWarps>;
     extern __shared__ uint4 smem_fold[];
     const int SC = P::S_STATE + p.ring_len * FoldPipeShape<ST, K>::RQ;
     uint4 *stage0 = smem_fold, *stage1 = smem_fold + SC;
@@ -278,7 +282,7 @@ __global__ void __launch_bounds__(PipeShape<ST, K>::NT, 2) k_fold_pipe(const Fol
         __syncthreads();
         if (done) {
             const int h = cur.hu / P::USL, us = cur.hu % P::USL;
-            tile_store<ST, K>(reinterpret_cast<ST *>(p.state) + (long long)cur.slot * p.st_slot +
+            tile_store<ST, K, PipeShape<ST, K, kFoldWarps>::NT, kFoldWarps>(reinterpret_cast<ST *>(p.state) + (long long)cur.slot * p.st_slot +
                                   (long long)h * p.st_head + us * P::CW,
                               p.st_k, s_cur);
         }
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(PipeShape<ST, K>::NT, 2) k_fold_pipe(const Fol
 }
 
 template <typename ST, int K> static cudaError_t launch_fold_pipe_t(const FoldParams &p, cudaStream_t st) {
-    using P = PipeShape<ST, K>;
+    using P = PipeShape<ST, K, kFoldWarps>;
     const int smem = 2 * (P::S_STATE + p.ring_len * FoldPipeShape<ST, K>::RQ) * 16;
     static int sms[64] = {0};
     static int occ[64][33] = {{0}};
@@ -331,10 +335,10 @@ template <typename ST, int K> static cudaError_t launch_rollback_t(const Rollbac
 }
 
 template <typename ST, int K> static cudaError_t launch_fold_any(const FoldParams &p, cudaStream_t s) {
-    if constexpr (PipeShape<ST, K>::OK) {
+    if constexpr (PipeShape<ST, K, kFoldWarps>::OK) {
         const bool aligned = (reinterpret_cast<uintptr_t>(p.ring) & 15u) == 0 && p.stride % 4 == 0 &&
                              p.u_off % 4 == 0;
-        if (aligned && (long long)p.batch * p.nv * PipeShape<ST, K>::USL < (1ll << 31))
+        if (aligned && (long long)p.batch * p.nv * PipeShape<ST, K, kFoldWarps>::USL < (1ll << 31))
             return launch_fold_pipe_t<ST, K>(p, s);
     }
     return launch_fold_t<ST, K>(p, s);

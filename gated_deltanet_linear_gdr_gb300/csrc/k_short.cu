@@ -21,8 +21,15 @@
 
 namespace gdr {
 
+// Warps per CTA budget of the short-row kernel (tile width = warps x 16 columns)
+// and CTAs per SM it is compiled for.
+constexpr int kShortWarps = 4;
+constexpr int kShortMinBlocks = 4;
+
+template <typename ST, int K> using ShortTile = PipeShape<ST, K, kShortWarps>;
+
 template <typename ST, int K> struct WinShape {
-    using P = PipeShape<ST, K>;                          // tile geometry (CW, CPR, S_STATE, USL)
+    using P = ShortTile<ST, K>;                          // tile geometry (CW, CPR, S_STATE, USL)
     static constexpr bool BF = sizeof(ST) == 2;
     static constexpr int LK = BF ? cmin(4, K / 8) : P::LK;  // lanes along K
     static constexpr int RG = K / 8 / LK;                // 8-row groups per lane
@@ -81,7 +88,7 @@ template <typename ST, int K>
 __device__ __forceinline__ void short_issue_tokens(const StepParams &p, const ShortMeta &m, int cb, int tc,
                                                    uint4 *stage) {
     using W = WinShape<ST, K>;
-    using P = PipeShape<ST, K>;
+    using P = ShortTile<ST, K>;
     constexpr int RQ = K / 4;  // raw chunks per q / k vector
     constexpr int RV = 2 * RQ + W::TV;
     const int h = m.hu / P::USL, us = m.hu % P::USL;
@@ -115,11 +122,11 @@ __device__ __forceinline__ void short_issue_tokens(const StepParams &p, const Sh
 template <typename ST, int K>
 __device__ __forceinline__ void short_issue(const StepParams &p, const ShortMeta &m, long long max_len,
                                             uint4 *stage) {
-    using P = PipeShape<ST, K>;
+    using P = ShortTile<ST, K>;
     using W = WinShape<ST, K>;
     if (short_unit_valid(p, m, max_len)) {
         const int h = m.hu / P::USL, us = m.hu % P::USL;
-        tile_issue<ST, K, W::NT>(reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
+        tile_issue<ST, K, W::NT, kShortWarps>(reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
                                      (long long)h * p.st_head + us * P::CW,
                                  p.st_k, stage);
         const int L = m.t1 - m.t0;
@@ -131,7 +138,7 @@ __device__ __forceinline__ void short_issue(const StepParams &p, const ShortMeta
 // This lane's C columns of tile row r (rows keep the 16-byte chunk swizzle).
 template <typename ST, int K>
 __device__ __forceinline__ ST *tile_cols(uint4 *tile, int r, int col) {
-    using P = PipeShape<ST, K>;
+    using P = ShortTile<ST, K>;
     constexpr int EPC = 16 / (int)sizeof(ST);
     return reinterpret_cast<ST *>(tile + r * P::CPR + ((col / EPC) ^ ((r >> 3) & (P::CPR - 1)))) + (col % EPC);
 }
@@ -156,7 +163,7 @@ __device__ __forceinline__ void short_put_tile(uint4 *tile, int r0, int col,
 template <typename ST, int K, Mode MODE>
 __device__ __forceinline__ bool short_compute(const StepParams &p, const RingParams &rp, const SnapParams &sp,
                                               long long max_len, const ShortMeta &m, uint4 *stage) {
-    using P = PipeShape<ST, K>;
+    using P = ShortTile<ST, K>;
     using W = WinShape<ST, K>;
     constexpr int V = K, NG = K / 8, LK = W::LK, RG = W::RG, ROWS = W::ROWS, C = W::C, NW = W::NW;
     constexpr int TCH = W::TCH;
@@ -385,7 +392,7 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
                     if (i < sp.n_inter) {
                         short_put_tile<ST, K>(stage, r0, col, s);
                         __syncthreads();
-                        tile_store<ST, K, W::NT>(reinterpret_cast<ST *>(sp.inter) + (long long)m.slot * sp.s_slot +
+                        tile_store<ST, K, W::NT, kShortWarps>(reinterpret_cast<ST *>(sp.inter) + (long long)m.slot * sp.s_slot +
                                                      (long long)i * sp.s_tok + (long long)h * sp.s_head +
                                                      us * P::CW,
                                                  V, stage);
@@ -405,10 +412,10 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
 }
 
 template <typename ST, int K, Mode MODE>
-__global__ void __launch_bounds__(WinShape<ST, K>::NT, 2)
+__global__ void __launch_bounds__(WinShape<ST, K>::NT, kShortMinBlocks)
     k_short(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len,
             const int nunits) {
-    using P = PipeShape<ST, K>;
+    using P = ShortTile<ST, K>;
     using W = WinShape<ST, K>;
     extern __shared__ uint4 smem_short[];
     uint4 *stage0 = smem_short, *stage1 = smem_short + W::SC;
@@ -428,7 +435,7 @@ __global__ void __launch_bounds__(WinShape<ST, K>::NT, 2)
         __syncthreads();
         if (commit) {
             const int h = cur.hu / P::USL, us = cur.hu % P::USL;
-            tile_store<ST, K, W::NT>(reinterpret_cast<ST *>(p.state) + (long long)cur.slot * p.st_slot +
+            tile_store<ST, K, W::NT, kShortWarps>(reinterpret_cast<ST *>(p.state) + (long long)cur.slot * p.st_slot +
                                          (long long)h * p.st_head + us * P::CW,
                                      p.st_k, s_cur);
         }
@@ -443,7 +450,7 @@ __global__ void __launch_bounds__(WinShape<ST, K>::NT, 2)
 template <typename ST, int K, Mode MODE>
 static cudaError_t launch_short_m(const StepParams &p, const RingParams &rp, const SnapParams &sp,
                                   long long max_len, cudaStream_t st) {
-    using P = PipeShape<ST, K>;
+    using P = ShortTile<ST, K>;
     using W = WinShape<ST, K>;
     constexpr int SMEM = 2 * W::SMEM1;
     static int configured[64] = {0};
@@ -470,8 +477,8 @@ static cudaError_t launch_short_m(const StepParams &p, const RingParams &rp, con
 }
 
 template <typename ST, int K> struct ShortOK {
-    static constexpr bool value = PipeShape<ST, K>::OK && WinShape<ST, K>::NT % PipeShape<ST, K>::CPR == 0 &&
-                                  PipeShape<ST, K>::S_STATE % WinShape<ST, K>::NT == 0 &&
+    static constexpr bool value = ShortTile<ST, K>::OK && WinShape<ST, K>::NT % ShortTile<ST, K>::CPR == 0 &&
+                                  ShortTile<ST, K>::S_STATE % WinShape<ST, K>::NT == 0 &&
                                   WinShape<ST, K>::NW >= 1;
 };
 
@@ -480,7 +487,7 @@ static cudaError_t launch_short_t(const StepParams &p, Mode mode, const RingPara
                                   long long max_len, cudaStream_t st, bool *used) {
     *used = false;
     if constexpr (ShortOK<ST, K>::value) {
-        if (!p.qkv_vec || (long long)p.batch * p.nv * PipeShape<ST, K>::USL >= (1ll << 31)) return cudaSuccess;
+        if (!p.qkv_vec || (long long)p.batch * p.nv * ShortTile<ST, K>::USL >= (1ll << 31)) return cudaSuccess;
         *used = true;
         switch (mode) {
             case Mode::Fwd: return launch_short_m<ST, K, Mode::Fwd>(p, rp, sp, max_len, st);

@@ -480,7 +480,7 @@ def run_gdr(args):
             "timed_wall_s": wall,
         },
         "roofline": {
-            "bound": "hbm", "kernel": "gdr::k_decode<bf16,128>", "achieved": achieved,
+            "bound": "hbm", "kernel": "gdr::k_decode_pipe<bf16,128,3>", "achieved": achieved,
             "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
             "peak_kind": f"{peak_kind} (STREAM-style copy)",
             "traffic": ncu_traffic("k_decode_bf16_128"),

@@ -81,6 +81,24 @@ struct RollbackParams {
 
 enum class Mode : int { Fwd = 0, Verify = 1, Snap = 2 };
 
+// Unsigned division by a divisor fixed at launch, as a multiply-high, an add
+// and a shift (Granlund and Montgomery, "Division by Invariant Integers using
+// Multiplication", 1994): with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (mulhi(n, m) + n) >> l for every 32-bit n (the add is done in 64 bits).
+struct FastDiv {
+    unsigned d, m, l;
+    FastDiv() = default;
+    __host__ explicit FastDiv(unsigned dd) : d(dd ? dd : 1u), m(0), l(0) {
+        while ((1ull << l) < d) ++l;
+        m = (unsigned)(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+    }
+#ifdef __CUDACC__
+    __device__ __forceinline__ unsigned div(unsigned n) const {
+        return (unsigned)(((unsigned long long)__umulhi(n, m) + n) >> l);
+    }
+#endif
+};
+
 // Launchers (defined next to their kernels).  Return cudaGetLastError().
 cudaError_t launch_decode(const StepParams &p, int K, bool bf16, cudaStream_t s);
 cudaError_t launch_chain(const StepParams &p, int K, bool bf16, Mode mode, const RingParams &rp,

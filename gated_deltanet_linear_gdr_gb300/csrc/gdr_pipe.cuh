@@ -50,10 +50,12 @@ __device__ __forceinline__ UnitMeta unit_meta(const StepParams &p, int u, int nu
 }
 
 // Asynchronous copy of one unit's state tile (K rows x CW columns starting at
-// src, rows st_k elements apart) into shared memory, swizzled.  Every thread
-// of the CTA takes S_STATE / NT chunks; consecutive threads read consecutive
-// 16-byte chunks of a row.
-template <typename ST, int K, int NT = PipeShape<ST, K>::NT, int NWMAX = 8>
+// src, rows st_k elements apart) into shared memory, swizzled: chunk c of row
+// r is stored at chunk c ^ ((r >> SWS) & (CPR - 1)).  SWS = 3 suits lanes that
+// own one 8-row group, SWS = 4 lanes that own runs of 16 or more rows.  Every
+// thread of the CTA takes S_STATE / NT chunks; consecutive threads read
+// consecutive 16-byte chunks of a row.
+template <typename ST, int K, int NT = PipeShape<ST, K>::NT, int NWMAX = 8, int SWS = 3>
 __device__ __forceinline__ void tile_issue(const ST *src, long long st_k, uint4 *tile) {
     using Sh = PipeShape<ST, K, NWMAX>;
     constexpr int CPR = Sh::CPR, RPI = NT / CPR, NJ = Sh::S_STATE / NT;
@@ -63,7 +65,7 @@ __device__ __forceinline__ void tile_issue(const ST *src, long long st_k, uint4 
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
         const int row = r0 + j * RPI;
-        cp_async16(tile + row * CPR + (c0 ^ ((row >> 3) & (CPR - 1))), src + (long long)j * RPI * st_k);
+        cp_async16(tile + row * CPR + (c0 ^ ((row >> SWS) & (CPR - 1))), src + (long long)j * RPI * st_k);
     }
 }
 
@@ -77,7 +79,7 @@ __device__ __forceinline__ uint4 *tile_lane_base(uint4 *tile, int kl, int col) {
 
 // Coalesced copy of a tile held in a stage to HBM: dst points at element
 // (row 0, column 0) of the unit's tile, rows st_k elements apart.
-template <typename ST, int K, int NT = PipeShape<ST, K>::NT, int NWMAX = 8>
+template <typename ST, int K, int NT = PipeShape<ST, K>::NT, int NWMAX = 8, int SWS = 3>
 __device__ __forceinline__ void tile_store(ST *dst, long long st_k, const uint4 *tile) {
     using Sh = PipeShape<ST, K, NWMAX>;
     constexpr int CPR = Sh::CPR, RPI = NT / CPR, NJ = Sh::S_STATE / NT;
@@ -86,7 +88,7 @@ __device__ __forceinline__ void tile_store(ST *dst, long long st_k, const uint4 
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
         const int row = r0 + j * RPI;
-        *reinterpret_cast<uint4 *>(dst + (long long)j * RPI * st_k) = tile[row * CPR + (c0 ^ ((row >> 3) & (CPR - 1)))];
+        *reinterpret_cast<uint4 *>(dst + (long long)j * RPI * st_k) = tile[row * CPR + (c0 ^ ((row >> SWS) & (CPR - 1)))];
     }
 }
 

@@ -4,8 +4,9 @@
 // row and keeps its K x VS piece of the state in registers in float32
 // ("gated_delta_recurrence_fwd_gpu" summary: the state stays in registers for
 // the whole sequence).  Each warp owns 16 of the columns and all K rows:
-// lane kl = lane % LK holds RG consecutive row groups (8*RG rows), lane
-// vl = lane / LK holds C columns.  The K-reductions of a token therefore end
+// lane kl = lane % LK holds RG consecutive row groups (8*RG rows, in the
+// row-pair form of gdr_state.cuh when RG is even), lane vl = lane / LK holds
+// C columns.  The K-reductions of a token therefore end
 // with log2(LK) xor-shuffles and the warps never wait for each other inside a
 // token.
 //
@@ -15,39 +16,41 @@
 // TC tokens.  One sweep over the state per token applies the update of token
 // t and accumulates the reductions of token t+1 (the readout identity in
 // gdr_device.cuh makes both reductions act on the pre-decay state).
-#include "gdr_device.cuh"
+#include "gdr_state.cuh"
 
 namespace gdr {
 
 template <typename ST, int K> struct ChainShape {
     static constexpr int V = K;
     static constexpr int NG = K / 8;               // row groups
-    static constexpr int LK = cmin(4, NG);         // lanes along K
+    static constexpr int LK = NG >= 4 ? cmin(4, NG / 2) : NG;  // lanes along K
     static constexpr int RG = NG / LK;             // groups per lane
+    static constexpr bool RPAIR = RG % 2 == 0;     // row-pair register form
     static constexpr int ROWS = RG * 8;            // rows per lane
     static constexpr int LV = 32 / LK;             // lanes along V
     static constexpr int C = cmin(2, V / LV);      // columns per lane
-    static constexpr int WC = LV * C;              // columns per warp (16)
+    static constexpr int WC = LV * C;              // columns per warp
     static constexpr int W = cmin(4, V / WC);      // warps per CTA
     static constexpr int NT = 32 * W;
     static constexpr int VS = W * WC;              // columns per CTA
     static constexpr int SLICES = V / VS;
     static constexpr int KP = K + LK * 4;          // padded staged vector length
     static constexpr int TC = 16;                  // tokens per staged chunk
+    static constexpr int NL = NG / (RPAIR ? 2 : 1);  // lanes per token when normalising
+    static constexpr int TPW = 32 / NL;            // tokens per warp when normalising
+    using State = LaneState<RG, C>;
 };
 
-// Padded shared-memory index of row i: 4 spare floats after each lane's run of
-// rows keeps the LK distinct 16-byte reads of one warp instruction in
-// different banks.
-template <int ROWS> __device__ __forceinline__ int pidx(int i) { return i + (i / ROWS) * 4; }
+// Shared-memory index of raw row i (natural order, padded every ROWS rows).
+template <int ROWS> __device__ __forceinline__ int pidx(int i) { return vpos<false, ROWS>(i); }
 
 template <typename ST, int K, Mode MODE>
-__global__ void __launch_bounds__(ChainShape<ST, K>::NT)
+__global__ void __launch_bounds__(ChainShape<ST, K>::NT, 4)
     k_chain(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len) {
     using Sh = ChainShape<ST, K>;
-    constexpr int V = K, NG = Sh::NG, LK = Sh::LK, RG = Sh::RG, ROWS = Sh::ROWS, C = Sh::C;
+    constexpr int V = K, LK = Sh::LK, ROWS = Sh::ROWS, C = Sh::C;
     constexpr int WC = Sh::WC, W = Sh::W, NT = Sh::NT, VS = Sh::VS, SLICES = Sh::SLICES;
-    constexpr int KP = Sh::KP, TC = Sh::TC;
+    constexpr int KP = Sh::KP, TC = Sh::TC, NL = Sh::NL, TPW = Sh::TPW;
 
     // two chunk buffers: chunk i+1 is copied in while chunk i is processed
     __shared__ __align__(16) float q_s[2][TC][KP];
@@ -109,13 +112,13 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
     // State piece: rows kl*ROWS .. +ROWS, columns col0 .. col0+C.
     ST *stile = reinterpret_cast<ST *>(p.state) + (long long)slot * p.st_slot +
                 (long long)h * p.st_head + (long long)(kl * ROWS) * p.st_k + col0;
-    float s[ROWS][C];
+    typename Sh::State s;
 #pragma unroll
     for (int i = 0; i < ROWS; ++i) {
         Pack<ST, C> x;
         x.load(stile + i * p.st_k);
 #pragma unroll
-        for (int c = 0; c < C; ++c) s[i][c] = x.get(c);
+        for (int c = 0; c < C; ++c) s.set(i, c, x.get(c));
     }
 
     const long long qoff = (long long)(hk * K) * p.qkv_cs;
@@ -177,74 +180,22 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
         float(*kb)[KP] = k_s[bi];
         float(*vb)[VS] = v_s[bi];
         float(*sb)[4] = sc_s[bi];
-        // ---- normalise: warp w takes tokens w, w+W, ...; lane l works on group l % NG
-        for (int tt = warp; tt < tc; tt += W) {
-            const int g = lane % NG;
-            const int o = pidx<ROWS>(g * 8);
-            float q8[8], k8[8];
-#pragma unroll
-            for (int i = 0; i < 8; i += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(&qb[tt][o + i]);
-                const float4 b4 = *reinterpret_cast<const float4 *>(&kb[tt][o + i]);
-                q8[i] = a4.x; q8[i + 1] = a4.y; q8[i + 2] = a4.z; q8[i + 3] = a4.w;
-                k8[i] = b4.x; k8[i + 1] = b4.y; k8[i + 2] = b4.z; k8[i + 3] = b4.w;
-            }
-            float ssq = chain_first(q8[0], q8[0]), ssk = chain_first(k8[0], k8[0]);
-            float kqr = chain_first(k8[0], q8[0]);
-#pragma unroll
-            for (int i = 1; i < 8; ++i) {
-                ssq = chain_next(q8[i], q8[i], ssq);
-                ssk = chain_next(k8[i], k8[i], ssk);
-                kqr = chain_next(k8[i], q8[i], kqr);
-            }
-            ssq = tree_lanes<NG>(ssq);
-            ssk = tree_lanes<NG>(ssk);
-            kqr = tree_lanes<NG>(kqr);
-            float inv_k, qsc, kq;
-            gdr_norm_scalars(ssq, ssk, kqr, p.l2norm, p.scale, p.eps, inv_k, qsc, kq);
-            const float alpha = gdr_alpha(sb[tt][0], p.decay_is_log);
-            __syncwarp();
-            if (lane < NG) {
-#pragma unroll
-                for (int i = 0; i < 8; i += 4) {
-                    *reinterpret_cast<float4 *>(&kb[tt][o + i]) =
-                        make_float4(__fmul_rn(k8[i], inv_k), __fmul_rn(k8[i + 1], inv_k),
-                                    __fmul_rn(k8[i + 2], inv_k), __fmul_rn(k8[i + 3], inv_k));
-                    *reinterpret_cast<float4 *>(&qb[tt][o + i]) =
-                        make_float4(__fmul_rn(q8[i], qsc), __fmul_rn(q8[i + 1], qsc),
-                                    __fmul_rn(q8[i + 2], qsc), __fmul_rn(q8[i + 3], qsc));
-                }
-            }
-            if (lane == 0) {
-                sb[tt][0] = alpha;
-                sb[tt][2] = kq;
-            }
+        // ---- normalise: NL lanes per token; warp w takes tokens w, w + W, ...
+        const bool rec_alpha = records && slice == 0, rec_k = rec_alpha && jr == 0;
+        for (int tb = 0; tb < tc; tb += W * TPW) {
+            const int tt = tb + warp + W * (lane / NL);
+            const bool act = tt < tc;
+            const int ts = act ? tt : 0;
+            float *rec = records ? ring_row + (long long)(cb + ts) * rp.stride : nullptr;
+            norm_token<K, Sh::RPAIR, ROWS>(qb[ts], kb[ts], sb[ts], lane % NL, act, p, rec_k ? rec : nullptr,
+                                           rec_alpha ? rec + rp.alpha_off + jr : nullptr);
         }
         __syncthreads();
 
         // ---- reductions of the chunk's first token
         const int rb = pidx<ROWS>(kl * ROWS);  // start of this lane's rows in the staged vectors
-        float pa[RG][C], pb[RG][C];
-#pragma unroll
-        for (int g = 0; g < RG; ++g) {
-#pragma unroll
-            for (int i4 = 0; i4 < 2; ++i4) {
-                const float4 kn = *reinterpret_cast<const float4 *>(&kb[0][rb + g * 8 + i4 * 4]);
-                const float4 qn = *reinterpret_cast<const float4 *>(&qb[0][rb + g * 8 + i4 * 4]);
-                const float knv[4] = {kn.x, kn.y, kn.z, kn.w}, qnv[4] = {qn.x, qn.y, qn.z, qn.w};
-#pragma unroll
-                for (int ii = 0; ii < 4; ++ii) {
-                    const int r = g * 8 + i4 * 4 + ii;
-                    if (i4 == 0 && ii == 0) {
-                        chain_first_cols<C>(s[r], knv[ii], pa[g]);
-                        chain_first_cols<C>(s[r], qnv[ii], pb[g]);
-                    } else {
-                        chain_next_cols<C>(s[r], knv[ii], pa[g]);
-                        chain_next_cols<C>(s[r], qnv[ii], pb[g]);
-                    }
-                }
-            }
-        }
+        float a[C], bq[C];
+        s.partials(&kb[0][rb], &qb[0][rb], a, bq);
 
         // ---- the chunk's tokens
         for (int tt = 0; tt < tc; ++tt) {
@@ -252,63 +203,25 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
             float u[C], o[C];
 #pragma unroll
             for (int c = 0; c < C; ++c) {
-                float ac[RG], bc[RG];
-#pragma unroll
-                for (int g = 0; g < RG; ++g) {
-                    ac[g] = pa[g][c];
-                    bc[g] = pb[g][c];
-                }
-                const float A = tree_lanes<LK>(tree<RG>(ac));
-                const float B = tree_lanes<LK>(tree<RG>(bc));
+                const float A = tree_lanes<LK>(a[c]);
+                const float B = tree_lanes<LK>(bq[c]);
                 u[c] = gdr_u(beta, alpha, A, vb[tt][wcol + c]);
                 o[c] = gdr_o(alpha, B, kq, u[c]);
             }
             const int step = cb + tt;  // token index inside the row
             if (kl == 0) store_f32<C>(obase + (long long)step * p.out_ss, p.out_vs, p.out_vec, o);
             if constexpr (MODE == Mode::Verify) {
-                if (records) {
-                    float *rec = ring_row + (long long)step * rp.stride;
-                    if (kl == 0) {
+                if (records && kl == 0) {
+                    float *rec = ring_row + (long long)step * rp.stride + rp.u_off + jr * V + col0;
 #pragma unroll
-                        for (int c = 0; c < C; ++c) rec[rp.u_off + jr * V + col0 + c] = u[c];
-                    }
-                    if (slice == 0) {
-                        if (tid == 0) rec[rp.alpha_off + jr] = alpha;
-                        if (jr == 0)
-                            for (int i = tid; i < K; i += NT) rec[i] = kb[tt][pidx<ROWS>(i)];
-                    }
+                    for (int c = 0; c < C; ++c) rec[c] = u[c];
                 }
             }
-            // One sweep: S <- k^_t u^T + alpha S, and token t+1's partials on the new S.
-            const bool next = tt + 1 < tc;
-#pragma unroll
-            for (int g = 0; g < RG; ++g) {
-#pragma unroll
-                for (int i4 = 0; i4 < 2; ++i4) {
-                    const int o4 = rb + g * 8 + i4 * 4;
-                    const float4 kc = *reinterpret_cast<const float4 *>(&kb[tt][o4]);
-                    const float kcv[4] = {kc.x, kc.y, kc.z, kc.w};
-                    float knv[4] = {0.f, 0.f, 0.f, 0.f}, qnv[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (next) {
-                        const float4 kn = *reinterpret_cast<const float4 *>(&kb[tt + 1][o4]);
-                        const float4 qn = *reinterpret_cast<const float4 *>(&qb[tt + 1][o4]);
-                        knv[0] = kn.x; knv[1] = kn.y; knv[2] = kn.z; knv[3] = kn.w;
-                        qnv[0] = qn.x; qnv[1] = qn.y; qnv[2] = qn.z; qnv[3] = qn.w;
-                    }
-#pragma unroll
-                    for (int ii = 0; ii < 4; ++ii) {
-                        const int r = g * 8 + i4 * 4 + ii;
-                        advance_cols<C>(s[r], kcv[ii], u, alpha);
-                        if (i4 == 0 && ii == 0) {
-                            chain_first_cols<C>(s[r], knv[ii], pa[g]);
-                            chain_first_cols<C>(s[r], qnv[ii], pb[g]);
-                        } else {
-                            chain_next_cols<C>(s[r], knv[ii], pa[g]);
-                            chain_next_cols<C>(s[r], qnv[ii], pb[g]);
-                        }
-                    }
-                }
-            }
+            // One sweep: S <- k^_t u^T + alpha S, and token t+1's partials on the new S
+            // (the chunk's last token sweeps against its own vectors; those partials
+            // are discarded and recomputed once the next chunk is normalised).
+            const int tn = tt + 1 < tc ? tt + 1 : tt;
+            s.advance_partials(&kb[tt][rb], &kb[tn][rb], &qb[tn][rb], u, alpha, a, bq);
             if constexpr (MODE == Mode::Snap) {
                 if ((step + 1) % sp.spt == 0) {
                     const int i = (step + 1) / sp.spt - 1;
@@ -320,7 +233,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
                         for (int r = 0; r < ROWS; ++r) {
                             Pack<ST, C> x;
 #pragma unroll
-                            for (int c = 0; c < C; ++c) x.set(c, s[r][c]);
+                            for (int c = 0; c < C; ++c) x.set(c, s.get(r, c));
                             x.store(it + r * V);
                         }
                     } else {
@@ -340,7 +253,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT)
         for (int i = 0; i < ROWS; ++i) {
             Pack<ST, C> x;
 #pragma unroll
-            for (int c = 0; c < C; ++c) x.set(c, s[i][c]);
+            for (int c = 0; c < C; ++c) x.set(c, s.get(i, c));
             x.store(stile + i * p.st_k);
         }
     }

@@ -247,11 +247,11 @@ template <int RG, int C> struct LaneState<RG, C, false> {
 // rows back pair-interleaved).  Every lane of the warp must call this
 // together (shuffles); lanes with act == false contribute zeros and write
 // nothing.  Writes k^ = k * inv_k and q~ = q * inv_q * scale in vpos order,
-// and, from lane gl == 0, ab[0] = alpha and ab[2] = k^ . q~.  ring_k (if not
-// null) receives k^ in natural order, ring_alpha (if not null) alpha.
+// and, from lane gl == 0, *kq_out = k^ . q~.  ring_k (if not null) receives
+// k^ in natural order.
 template <int K, bool RPAIR, int PADROWS>
-__device__ __forceinline__ void norm_token(float *q, float *k, float *ab, int gl, bool act, const StepParams &p,
-                                           float *ring_k, float *ring_alpha) {
+__device__ __forceinline__ void norm_token(float *q, float *k, float *kq_out, int gl, bool act, const StepParams &p,
+                                           float *ring_k) {
     constexpr int GPL = RPAIR ? 2 : 1, NL = K / 8 / GPL, NR = 8 * GPL;
     static_assert(PADROWS % NR == 0, "a lane's rows must not straddle padding");
     const int r0 = gl * NR;
@@ -306,12 +306,7 @@ __device__ __forceinline__ void norm_token(float *q, float *k, float *ab, int gl
         for (int m = 0; m < NR; m += 4)
             *reinterpret_cast<float4 *>(ring_k + r0 + m) = make_float4(kn[m], kn[m + 1], kn[m + 2], kn[m + 3]);
     }
-    if (gl == 0) {
-        const float alpha = gdr_alpha(ab[0], p.decay_is_log);
-        ab[0] = alpha;
-        ab[2] = kq;
-        if (ring_alpha) *ring_alpha = alpha;
-    }
+    if (gl == 0) *kq_out = kq;
 }
 
 }  // namespace gdr

@@ -187,8 +187,12 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT, 4)
             const bool act = tt < tc;
             const int ts = act ? tt : 0;
             float *rec = records ? ring_row + (long long)(cb + ts) * rp.stride : nullptr;
-            norm_token<K, Sh::RPAIR, ROWS>(qb[ts], kb[ts], sb[ts], lane % NL, act, p, rec_k ? rec : nullptr,
-                                           rec_alpha ? rec + rp.alpha_off + jr : nullptr);
+            norm_token<K, Sh::RPAIR, ROWS>(qb[ts], kb[ts], &sb[ts][2], lane % NL, act, p, rec_k ? rec : nullptr);
+            if (act && lane % NL == 0) {
+                const float alpha = gdr_alpha(sb[ts][0], p.decay_is_log);
+                sb[ts][0] = alpha;
+                if (rec_alpha) rec[rp.alpha_off + jr] = alpha;
+            }
         }
         __syncthreads();
 

@@ -143,181 +143,124 @@ __global__ void __launch_bounds__(kFoldThreads) k_rollback(const RollbackParams 
 }
 
 // ---------------------------------------------------------------------------
-// Pipelined fold for the common layouts: persistent CTAs walk (row, head,
-// tile) units; a unit's stage holds its state tile and its first `count`
-// records (k^, the tile's u columns, alpha), copied with cp.async while the
-// previous unit computes; the new tile leaves through the stage as coalesced
-// rows.  Lane layout and arithmetic as the other pipelined kernels.
+// Fold for the common layouts.  The advance has no reduction, so a unit is
+// (row, head, KT-row slice): KT consecutive state rows with all V columns, one
+// contiguous block of memory (16 KiB at K = V = 128).  Thread t owns R rows x
+// C columns (one 16-byte vector per row): rows (t / LV) * R .. + R - 1,
+// columns (t % LV) * C .. + C - 1, so a warp's loads and stores cover whole
+// rows.
 
-// Warps per CTA (tile width) and CTAs per SM of the pipelined fold.
-constexpr int kFoldWarps = 4;
-constexpr int kFoldMinBlocks = 4;
-
-struct FoldMeta {
-    int hu, c, slot, rs;  // c == 0: nothing to do
+template <typename ST, int K, int NTT> struct FoldTile {
+    static constexpr int V = K;
+    static constexpr int NT = NTT;                                  // threads per CTA
+    static constexpr int C = 16 / (int)sizeof(ST);                  // columns per thread
+    static constexpr int LV = V / C;                                // threads along a row
+    static constexpr int LKR = NT / LV;                             // threads along K
+    static constexpr int KT = cmin(K, 16384 / (V * (int)sizeof(ST)));  // rows per unit
+    static constexpr int R = KT / LKR;                              // rows per thread
+    static constexpr int KS = K / KT;                               // units per (row, head)
+    static constexpr int RQ = KT / 4 + V / 4 + 1;                   // 16-byte chunks per staged record
+    static constexpr bool OK = LV <= NT && R >= 1 && K % KT == 0;
 };
 
-template <int USL>
-__device__ __forceinline__ FoldMeta fold_meta(const FoldParams &p, long long u, int nunits) {
-    FoldMeta m{};
-    if (u >= nunits) return m;
-    const int ui = (int)u;
-    const int b = ui / USL / p.nv;
-    m.hu = ui - b * p.nv * USL;
-    m.c = p.counts[b];
-    m.slot = p.slot_idx[b];
-    m.rs = p.ring_slot[b];
-    return m;
-}
-
-__device__ __forceinline__ bool fold_active(const FoldParams &p, const FoldMeta &m) {
-    return m.c >= 1 && m.c <= p.ring_len && m.slot >= 0 && m.slot < p.max_slots && m.rs >= 0 &&
-           m.rs < p.ring_rows;
-}
-
-template <typename ST, int K> struct FoldPipeShape {
-    using P = PipeShape<ST, K, kFoldWarps>;
-    static constexpr int RQ = K / 4 + P::CW / 4 + 1;  // 16-byte chunks per staged record
-};
+// One CTA per unit: the CTA's rows go straight to registers (its R 16-byte
+// loads per thread issued first), the unit's first `count` records (the
+// slice's k^, the head's u, alpha) to shared memory with cp.async meanwhile;
+// after one barrier every thread advances its rows and stores them.  Many CTAs
+// per SM keep enough loads in flight without a software pipeline.
+constexpr int kFoldDirectThreads = 256;
 
 template <typename ST, int K>
-__device__ __forceinline__ void fold_issue(const FoldParams &p, const FoldMeta &m, uint4 *stage) {
-    using P = PipeShape<ST, K, kFoldWarps>;
-    using F = FoldPipeShape<ST, K>;
-    if (fold_active(p, m)) {
-        const int h = m.hu / P::USL, us = m.hu % P::USL;
-        tile_issue<ST, K, PipeShape<ST, K, kFoldWarps>::NT, kFoldWarps>(reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
-                              (long long)h * p.st_head + us * P::CW,
-                          p.st_k, stage);
-        const int hk = h / p.r, jr = h % p.r;
-        const float *rrow = p.ring + ((long long)m.rs * p.nk + hk) * p.ring_len * p.stride;
-        uint4 *recs = stage + P::S_STATE;
-        constexpr int RV = K / 4 + P::CW / 4;  // vector chunks per record
-        for (int ch = threadIdx.x; ch < m.c * RV; ch += P::NT) {
+__global__ void __launch_bounds__(kFoldDirectThreads) k_fold_direct(const FoldParams p) {
+    using F = FoldTile<ST, K, kFoldDirectThreads>;
+    constexpr int C = F::C, R = F::R;
+    using VT = typename Pack<ST, C>::VT;
+    extern __shared__ uint4 smem_fd[];
+    const long long u = blockIdx.x;
+    const long long bq = u / F::KS;
+    const int b = (int)(bq / p.nv);
+    const int hs = (int)(u - (long long)b * p.nv * F::KS);  // h * KS + ks
+    const int h = hs / F::KS, ks = hs % F::KS;
+    const int c = p.counts[b], slot = p.slot_idx[b], rs = p.ring_slot[b];
+    const int tid = threadIdx.x;
+    const bool leader = tid == 0 && hs == 0;
+    if (c == 0 || slot == -1 || c > p.ring_len) return;
+    if (c < 0) {
+        if (leader) flag(p.status, GDR_STATUS_BAD_COUNT);
+        return;
+    }
+    if (slot < 0 || slot >= p.max_slots) {
+        if (leader) flag(p.status, GDR_STATUS_BAD_SLOT);
+        return;
+    }
+    if (rs < 0 || rs >= p.ring_rows) {
+        if (leader) flag(p.status, GDR_STATUS_BAD_RING_SLOT);
+        return;
+    }
+    const int cg = tid % F::LV, r0 = (tid / F::LV) * R;
+    ST *rows = reinterpret_cast<ST *>(p.state) + (long long)slot * p.st_slot + (long long)h * p.st_head +
+               (long long)(ks * F::KT + r0) * p.st_k + cg * C;
+    VT raw[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) raw[i] = *reinterpret_cast<const VT *>(rows + (long long)i * p.st_k);
+    // records -> shared memory: per record RQ chunks [k^ slice | u | alpha]
+    const int jr = h % p.r;
+    {
+        const int hk = h / p.r;
+        const float *rrow = p.ring + ((long long)rs * p.nk + hk) * p.ring_len * p.stride;
+        constexpr int RV = F::KT / 4 + K / 4;
+        for (int ch = tid; ch < c * RV; ch += F::NT) {
             const int t = ch / RV, r = ch - t * RV;
             const float *rec = rrow + (long long)t * p.stride;
-            const float *g = r < K / 4 ? rec + 4 * r : rec + p.u_off + jr * K + us * P::CW + 4 * (r - K / 4);
-            cp_async16(recs + t * F::RQ + r, g);
+            const float *g = r < F::KT / 4 ? rec + ks * F::KT + 4 * r : rec + p.u_off + jr * K + 4 * (r - F::KT / 4);
+            cp_async16(smem_fd + t * F::RQ + r, g);
         }
-        for (int t = threadIdx.x; t < m.c; t += P::NT)
-            cp_async4(recs + t * F::RQ + RV, rrow + (long long)t * p.stride + p.alpha_off + jr);
+        for (int t = tid; t < c; t += F::NT)
+            cp_async4(smem_fd + t * F::RQ + RV, rrow + (long long)t * p.stride + p.alpha_off + jr);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
     }
-    cp_async_commit();
-}
-
-template <typename ST, int K>
-__device__ __forceinline__ bool fold_compute(const FoldParams &p, const FoldMeta &m, uint4 *stage) {
-    using P = PipeShape<ST, K, kFoldWarps>;
-    using F = FoldPipeShape<ST, K>;
-    constexpr int LK = P::LK, C = P::C, CPR = P::CPR;
-    using VT = typename Pack<ST, C>::VT;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool leader = tid == 0 && m.hu == 0;
-    if (m.c == 0 || m.slot == -1 || m.c > p.ring_len) return false;
-    if (m.c < 0) {
-        if (leader) flag(p.status, GDR_STATUS_BAD_COUNT);
-        return false;
-    }
-    if (m.slot < 0 || m.slot >= p.max_slots) {
-        if (leader) flag(p.status, GDR_STATUS_BAD_SLOT);
-        return false;
-    }
-    if (m.rs < 0 || m.rs >= p.ring_rows) {
-        if (leader) flag(p.status, GDR_STATUS_BAD_RING_SLOT);
-        return false;
-    }
-    const int kl = lane % LK, vl = lane / LK;
-    const int col = warp * P::WC + vl * C;
-    uint4 *mine = tile_lane_base<ST, K, kFoldWarps>(stage, kl, col);
-    float s[8][C];
+    float s[R][C];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < R; ++i) {
         Pack<ST, C> x;
-        x.u.v = *reinterpret_cast<const VT *>(mine + i * CPR);
+        x.u.v = raw[i];
 #pragma unroll
         for (int cc = 0; cc < C; ++cc) s[i][cc] = x.get(cc);
     }
-    const float *recs = reinterpret_cast<const float *>(stage + P::S_STATE);
-    for (int t = 0; t < m.c; ++t) {
+    const float *recs = reinterpret_cast<const float *>(smem_fd);
+    for (int t = 0; t < c; ++t) {
         const float *rec = recs + t * F::RQ * 4;
-        const float alpha = rec[K + P::CW];
-        float kh[8], u[C];
+        const float alpha = rec[F::KT + K];
+        float kh[R], uu[C];
+        if constexpr (R % 4 == 0) {
 #pragma unroll
-        for (int i = 0; i < 8; i += 4) {
-            const float4 a4 = *reinterpret_cast<const float4 *>(rec + kl * 8 + i);
-            kh[i] = a4.x; kh[i + 1] = a4.y; kh[i + 2] = a4.z; kh[i + 3] = a4.w;
+            for (int i = 0; i < R; i += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(rec + r0 + i);
+                kh[i] = a4.x; kh[i + 1] = a4.y; kh[i + 2] = a4.z; kh[i + 3] = a4.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < R; ++i) kh[i] = rec[r0 + i];
         }
 #pragma unroll
         for (int cc = 0; cc < C; cc += 4) {
-            const float4 b4 = *reinterpret_cast<const float4 *>(rec + K + col + cc);
-            u[cc] = b4.x; u[cc + 1] = b4.y; u[cc + 2] = b4.z; u[cc + 3] = b4.w;
+            const float4 b4 = *reinterpret_cast<const float4 *>(rec + F::KT + cg * C + cc);
+            uu[cc] = b4.x; uu[cc + 1] = b4.y; uu[cc + 2] = b4.z; uu[cc + 3] = b4.w;
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) advance_cols<C>(s[i], kh[i], u, alpha);
+        for (int i = 0; i < R; ++i) advance_cols<C>(s[i], kh[i], uu, alpha);
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) pack_store<ST, C>(mine + i * CPR, s[i]);
-    return true;
+    for (int i = 0; i < R; ++i) pack_store<ST, C>(reinterpret_cast<uint4 *>(rows + (long long)i * p.st_k), s[i]);
 }
 
-template <typename ST, int K>
-__global__ void __launch_bounds__(PipeShape<ST, K, kFoldWarps>::NT, kFoldMinBlocks) k_fold_pipe(const FoldParams p, const int nunits) {
-    using P = PipeShape<ST, K, kFoldWarps>;
-    extern __shared__ uint4 smem_fold[];
-    const int SC = P::S_STATE + p.ring_len * FoldPipeShape<ST, K>::RQ;
-    uint4 *stage0 = smem_fold, *stage1 = smem_fold + SC;
-    const long long G = gridDim.x;
-    FoldMeta cur = fold_meta<P::USL>(p, blockIdx.x, nunits);
-    fold_issue<ST, K>(p, cur, stage0);
-    FoldMeta nxt = fold_meta<P::USL>(p, (long long)blockIdx.x + G, nunits);
-    int sel = 0;
-    for (long long u = blockIdx.x; u < nunits; u += G) {
-        uint4 *s_cur = sel ? stage1 : stage0;
-        uint4 *s_nxt = sel ? stage0 : stage1;
-        fold_issue<ST, K>(p, nxt, s_nxt);
-        const FoldMeta later = fold_meta<P::USL>(p, u + 2 * G, nunits);
-        cp_async_wait<1>();
-        __syncthreads();
-        const bool done = fold_compute<ST, K>(p, cur, s_cur);
-        __syncthreads();
-        if (done) {
-            const int h = cur.hu / P::USL, us = cur.hu % P::USL;
-            tile_store<ST, K, PipeShape<ST, K, kFoldWarps>::NT, kFoldWarps>(reinterpret_cast<ST *>(p.state) + (long long)cur.slot * p.st_slot +
-                                  (long long)h * p.st_head + us * P::CW,
-                              p.st_k, s_cur);
-        }
-        __syncthreads();
-        cur = nxt;
-        nxt = later;
-        sel ^= 1;
-    }
-    cp_async_wait<0>();
-}
-
-template <typename ST, int K> static cudaError_t launch_fold_pipe_t(const FoldParams &p, cudaStream_t st) {
-    using P = PipeShape<ST, K, kFoldWarps>;
-    const int smem = 2 * (P::S_STATE + p.ring_len * FoldPipeShape<ST, K>::RQ) * 16;
-    static int sms[64] = {0};
-    static int occ[64][33] = {{0}};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!occ[dev][p.ring_len]) {
-        e = cudaFuncSetAttribute(k_fold_pipe<ST, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 2 * (P::S_STATE + 32 * FoldPipeShape<ST, K>::RQ) * 16);
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        int o = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k_fold_pipe<ST, K>, P::NT, smem);
-        if (e != cudaSuccess) return e;
-        occ[dev][p.ring_len] = o < 1 ? 1 : o;
-    }
-    const long long nunits = (long long)p.batch * p.nv * P::USL;
-    long long grid = (long long)sms[dev] * occ[dev][p.ring_len];
-    if (grid > nunits) grid = nunits;
-    if (grid > 0) k_fold_pipe<ST, K><<<(unsigned)grid, P::NT, smem, st>>>(p, (int)nunits);
+template <typename ST, int K> static cudaError_t launch_fold_direct_t(const FoldParams &p, cudaStream_t st) {
+    using F = FoldTile<ST, K, kFoldDirectThreads>;
+    const int smem = p.ring_len * F::RQ * 16;
+    const long long blocks = (long long)p.batch * p.nv * F::KS;
+    if (blocks > 0) k_fold_direct<ST, K><<<(unsigned)blocks, F::NT, smem, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -335,11 +278,11 @@ template <typename ST, int K> static cudaError_t launch_rollback_t(const Rollbac
 }
 
 template <typename ST, int K> static cudaError_t launch_fold_any(const FoldParams &p, cudaStream_t s) {
-    if constexpr (PipeShape<ST, K, kFoldWarps>::OK) {
-        const bool aligned = (reinterpret_cast<uintptr_t>(p.ring) & 15u) == 0 && p.stride % 4 == 0 &&
-                             p.u_off % 4 == 0;
-        if (aligned && (long long)p.batch * p.nv * PipeShape<ST, K, kFoldWarps>::USL < (1ll << 31))
-            return launch_fold_pipe_t<ST, K>(p, s);
+    const bool aligned = (reinterpret_cast<uintptr_t>(p.ring) & 15u) == 0 && p.stride % 4 == 0 &&
+                         p.u_off % 4 == 0;
+    if constexpr (FoldTile<ST, K, kFoldDirectThreads>::OK) {
+        if (aligned && (long long)p.batch * p.nv * FoldTile<ST, K, kFoldDirectThreads>::KS < (1ll << 31))
+            return launch_fold_direct_t<ST, K>(p, s);
     }
     return launch_fold_t<ST, K>(p, s);
 }

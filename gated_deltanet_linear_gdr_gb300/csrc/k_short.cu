@@ -271,8 +271,13 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
             const bool act = tt < tc;
             float *tq = tokf + (act ? tt : 0) * W::TOK * 4;
             float *rec = records ? ring_row + (long long)(cb + (act ? tt : 0)) * rp.stride : nullptr;
-            norm_token<K, true, ROWS>(tq, tq + W::KP, tq + W::TOKV * 4, lane % NL, act, p,
-                                      rec_k ? rec : nullptr, rec_alpha ? rec + rp.alpha_off + jr : nullptr);
+            float *ab = tq + W::TOKV * 4;
+            norm_token<K, true, ROWS>(tq, tq + W::KP, ab + 2, lane % NL, act, p, rec_k ? rec : nullptr);
+            if (act && lane % NL == 0) {
+                const float alpha = gdr_alpha(ab[0], p.decay_is_log);
+                ab[0] = alpha;
+                if (rec_alpha) rec[rp.alpha_off + jr] = alpha;
+            }
         }
         __syncthreads();
 

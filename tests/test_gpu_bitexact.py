@@ -59,9 +59,11 @@ def test_verify_output_equals_forward_and_pool_untouched(state_dtype):
             assert (host[s] == pool[s]).all(), "verify must leave the pool alone"
 
 
+@pytest.mark.parametrize("K", [32, 64, 128])
 @pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
-def test_verify_plus_fold_equals_forward_over_prefix(state_dtype):
-    w = W.verify_fold(batch=24, max_slots=48, ring_rows=48, state_dtype=state_dtype)
+def test_verify_plus_fold_equals_forward_over_prefix(state_dtype, K):
+    kw = {} if K == 128 else dict(nk=2, nv=4, K=K)
+    w = W.verify_fold(batch=24, max_slots=48, ring_rows=48, state_dtype=state_dtype, **kw)
     counts = np.array([b % 6 for b in range(w.batch)], np.int32)
     counts[-1] = w.row_lengths[-1]
     w = dataclasses.replace(w, counts=counts)
@@ -333,11 +335,13 @@ def test_short_row_kernel_equals_general_kernel(state_dtype):
     assert st == 0, gdr.status_names(st)  # the 20-token row has exactly n_inter = 6 drafts of 3
 
 
+@pytest.mark.parametrize("K", [16, 32, 64, 128])
 @pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
-def test_pipelined_fold_equals_simple_fold(state_dtype):
-    """A 16-byte-aligned ring takes the pipelined fold, a view offset by one
-    float takes the simple one: same bits."""
-    w = W.verify_fold(batch=40, max_slots=64, ring_rows=64, state_dtype=state_dtype)
+def test_sliced_fold_equals_simple_fold(state_dtype, K):
+    """A 16-byte-aligned ring takes the row-slice fold (where the head size
+    allows it), a view offset by one float takes the simple one: same bits."""
+    kw = {} if K == 128 else dict(nk=2, nv=6, K=K)
+    w = W.verify_fold(batch=40, max_slots=64, ring_rows=64, state_dtype=state_dtype, **kw)
     pool = w.state_pool()
     d = Dev(w, pool)
     ring = ring_for(w, w.ring_len, w.ring_rows)

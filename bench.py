@@ -172,6 +172,15 @@ def fma_ops(head_tokens, K, V, per=4):
     return head_tokens * per * K * V
 
 
+def fp32_fma_peak(dev):
+    """FMA-pipe operations per second: SMs x 128 lanes x SM clock (2.07 GHz
+    when the device does not report its clock)."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    clk = getattr(props, "clock_rate", 0) * 1e3 or 2.07e9
+    return props.multi_processor_count * 128 * clk
+
+
 # ------------------------------------------------------------- GPU side ---
 
 class DecodeStep:
@@ -262,9 +271,7 @@ def bench_prefill(dev, flush, stream, hbm_peak, steps):
         fn()
     ms = statistics.median(time_steps(fn, max(3, steps // 10), flush, stream))
     ht = w.live_head_tokens
-    props = torch.cuda.get_device_properties(dev)
-    clk = props.clock_rate * 1e3 if hasattr(props, "clock_rate") else 2.07e9
-    fp32_peak = props.multi_processor_count * 128 * clk
+    fp32_peak = fp32_fma_peak(dev)
     return {
         "workload": f"ragged prefill: {w.batch} rows, lengths {w.row_lengths.min()}..{w.row_lengths.max()}"
                     f" (T={w.total_tokens}), nk=16, nv=32, K=V=128, bf16 pool [16,32,128,128]",
@@ -309,6 +316,11 @@ def bench_verify_fold(dev, flush, stream, hbm_peak, steps):
     fbytes = (int(active.sum()) * w.nv * w.K * w.V * 2 * 2
               + int(w.counts[active].sum()) * w.nk * rec * 4)
     ht = w.live_head_tokens
+    # roofline time of each kernel: the larger of its HBM time and its FMA-pipe time
+    fp32_peak = fp32_fma_peak(dev)
+    v_roof = max(vbytes / (hbm_peak * 1e9), fma_ops(ht, w.K, w.V) / fp32_peak)
+    f_roof = max(fbytes / (hbm_peak * 1e9),
+                 fma_ops(int(w.counts[active].sum()) * w.nv, w.K, w.V, per=2) / fp32_peak)
     return {
         "workload": "verify: 127 rows x 5 drafts + 1 row of 12, RING_LEN 8, nk=16, nv=32, "
                     "K=V=128, bf16 pool [256,32,128,128], fp32 ring [256,16,8,388]; then fold "
@@ -316,6 +328,8 @@ def bench_verify_fold(dev, flush, stream, hbm_peak, steps):
         "verify_ms": tv, "fold_ms": tf, "head_tokens_per_s": ht / ((tv + tf) * 1e-3),
         "verify_hbm_gbs": vbytes / (tv * 1e-3) / 1e9, "fold_hbm_gbs": fbytes / (tf * 1e-3) / 1e9,
         "frac_hbm_verify_plus_fold": (vbytes + fbytes) / ((tv + tf) * 1e-3) / 1e9 / hbm_peak,
+        "roofline_us_verify": v_roof * 1e6, "roofline_us_fold": f_roof * 1e6,
+        "frac_roofline_verify_plus_fold": (v_roof + f_roof) / ((tv + tf) * 1e-3),
     }
 
 

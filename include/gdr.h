@@ -143,8 +143,9 @@ int gdr_output_shape(int64_t total_tokens, int32_t nv, int32_t V, int64_t out_sh
 /* Minimum ring record length in elements for GQA ratio `ratio` = nv/nk
  * ("gated_delta_recurrence_verify_ring_gpu", ring_record_stride: at least
  * gated_delta_ring_record_elements(nv // nk)).  Record layout, float32:
- *     [ k^ (K) | alpha_0 .. alpha_{ratio-1}, zero-padded to a multiple of 4 |
+ *     [ k^ (K) | alpha_0 .. alpha_{ratio-1}, padded to a multiple of 4 |
  *       u_0 (V) | ... | u_{ratio-1} (V) ]
+ * (the padding floats are never written or read)
  * where u_j and alpha_j belong to value head hk*ratio + j.  Returns the length
  * (K + 4*ceil(ratio/4) + ratio*V) or a negative code. */
 int gdr_ring_record_elements(int32_t K, int32_t V, int32_t ratio);

@@ -46,14 +46,17 @@ template <int RG, int C> struct LaneState<RG, C, true> {
             x[r >> 4][r & 7][c].x = v;
     }
 
+    // Row pairs i = 2m and 2m + 1 of group pair gp from the lane's staged vector v.
+    static __device__ __forceinline__ void pair2(const float *v, int gp, int m, float2 &a, float2 &b) {
+        const float4 t = *reinterpret_cast<const float4 *>(v + gp * 16 + 4 * m);
+        a = make_float2(t.x, t.y);
+        b = make_float2(t.z, t.w);
+    }
+
     // Eight row pairs of group pair gp from the lane's staged vector v.
     static __device__ __forceinline__ void pairs(const float *v, int gp, float2 (&o)[8]) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float4 t = *reinterpret_cast<const float4 *>(v + gp * 16 + 4 * m);
-            o[2 * m] = make_float2(t.x, t.y);
-            o[2 * m + 1] = make_float2(t.z, t.w);
-        }
+        for (int m = 0; m < 4; ++m) pair2(v, gp, m, o[2 * m], o[2 * m + 1]);
     }
 
     static __device__ __forceinline__ void fold_tree(const float2 (&pa)[NP][C], const float2 (&pb)[NP][C],
@@ -74,25 +77,33 @@ template <int RG, int C> struct LaneState<RG, C, true> {
     }
 
     // In-thread part of a = S^T kv and b = S^T qv: the lane's group chains
-    // combined by the first log2(RG) tree levels.
+    // combined by the first log2(RG) tree levels.  Rows advance in the outer
+    // loop so that every step issues the 2 NP C independent chains together.
     __device__ __forceinline__ void partials(const float *kv, const float *qv, float (&a)[C], float (&b)[C]) const {
         float2 pa[NP][C], pb[NP][C];
 #pragma unroll
-        for (int gp = 0; gp < NP; ++gp) {
-            float2 kp[8], qp[8];
-            pairs(kv, gp, kp);
-            pairs(qv, gp, qp);
+        for (int m = 0; m < 4; ++m) {
+            float2 kp[NP][2], qp[NP][2];
 #pragma unroll
-            for (int c = 0; c < C; ++c) {
-                pa[gp][c] = __fmul2_rn(x[gp][0][c], kp[0]);
-                pb[gp][c] = __fmul2_rn(x[gp][0][c], qp[0]);
+            for (int gp = 0; gp < NP; ++gp) {
+                pair2(kv, gp, m, kp[gp][0], kp[gp][1]);
+                pair2(qv, gp, m, qp[gp][0], qp[gp][1]);
             }
 #pragma unroll
-            for (int i = 1; i < 8; ++i) {
+            for (int ii = 0; ii < 2; ++ii) {
+                const int i = 2 * m + ii;
 #pragma unroll
-                for (int c = 0; c < C; ++c) {
-                    pa[gp][c] = __ffma2_rn(x[gp][i][c], kp[i], pa[gp][c]);
-                    pb[gp][c] = __ffma2_rn(x[gp][i][c], qp[i], pb[gp][c]);
+                for (int gp = 0; gp < NP; ++gp) {
+#pragma unroll
+                    for (int c = 0; c < C; ++c) {
+                        if (i == 0) {
+                            pa[gp][c] = __fmul2_rn(x[gp][0][c], kp[gp][0]);
+                            pb[gp][c] = __fmul2_rn(x[gp][0][c], qp[gp][0]);
+                        } else {
+                            pa[gp][c] = __ffma2_rn(x[gp][i][c], kp[gp][ii], pa[gp][c]);
+                            pb[gp][c] = __ffma2_rn(x[gp][i][c], qp[gp][ii], pb[gp][c]);
+                        }
+                    }
                 }
             }
         }

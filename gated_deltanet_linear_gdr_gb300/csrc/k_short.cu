@@ -23,22 +23,25 @@
 
 namespace gdr {
 
-// Warps per CTA budget of the short-row kernel (tile width = warps x 16 columns)
-// and CTAs per SM it is compiled for.
-constexpr int kShortWarps = 4;
-constexpr int kShortMinBlocks = 4;
+// Tile width of the short-row kernel (kShortTileWarps x 16 columns), lanes
+// along K for bf16 pools (the warps per CTA follow: tile width / (32 / LK x 2
+// columns)), and CTAs per SM it is compiled for.
+constexpr int kShortTileWarps = 4;
+constexpr int kShortLKbf16 = 4;
+constexpr int kShortMinBlocksBf16 = 4;
+constexpr int kShortMinBlocksF32 = 4;
 
 // Tile swizzle shift: a lane owns 16 (f32) or 32 (bf16) consecutive rows, so
 // the row's 16-row block picks the chunk permutation (conflict-free reads).
 constexpr int kShortSwizzle = 4;
 
-template <typename ST, int K> using ShortTile = PipeShape<ST, K, kShortWarps>;
+template <typename ST, int K> using ShortTile = PipeShape<ST, K, kShortTileWarps>;
 
 template <typename ST, int K> struct WinShape {
     using P = ShortTile<ST, K>;                          // tile geometry (CW, CPR, S_STATE, USL)
     static constexpr bool BF = sizeof(ST) == 2;
     static constexpr int NG = K / 8;
-    static constexpr int LK = BF ? cmin(4, K / 16) : K / 16;  // lanes along K
+    static constexpr int LK = BF ? cmin(kShortLKbf16, K / 16) : K / 16;  // lanes along K
     static constexpr int RG = NG / LK;                   // 8-row groups per lane (even)
     static constexpr int ROWS = 8 * RG;
     static constexpr int LV = 32 / LK;
@@ -55,6 +58,7 @@ template <typename ST, int K> struct WinShape {
     static constexpr int SMEM1 = SC * 16;
     static constexpr int NL = NG / 2;                    // lanes per token when normalising
     static constexpr int TPW = 32 / NL;                  // tokens per warp when normalising
+    static constexpr int MINB = BF ? kShortMinBlocksBf16 : kShortMinBlocksF32;  // CTAs per SM
     using State = LaneState<RG, C>;
     static_assert(RG % 2 == 0, "row-pair form");
 };
@@ -138,7 +142,7 @@ __device__ __forceinline__ void short_issue(const StepParams &p, const ShortMeta
     using P = ShortTile<ST, K>;
     using W = WinShape<ST, K>;
     if (short_unit_valid(p, m, max_len)) {
-        tile_issue<ST, K, W::NT, kShortWarps, kShortSwizzle>(reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
+        tile_issue<ST, K, W::NT, kShortTileWarps, kShortSwizzle>(reinterpret_cast<const ST *>(p.state) + (long long)m.slot * p.st_slot +
                                      (long long)m.h * p.st_head + m.us * P::CW,
                                  p.st_k, stage);
         const int L = m.t1 - m.t0;
@@ -265,9 +269,11 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
             cp_async_wait<0>();
             __syncthreads();
         }
-        // normalise: NL lanes per token; warp w takes tokens w, w + NW, ...
+        // normalise: NL lanes per token, TPW tokens per warp, packed into the
+        // low warps (a warp with no token skips the pass)
         for (int tb = 0; tb < tc; tb += NW * TPW) {
-            const int tt = tb + warp + NW * (lane / NL);
+            if (tb + TPW * warp >= tc) continue;  // uniform over the warp
+            const int tt = tb + TPW * warp + lane / NL;
             const bool act = tt < tc;
             float *tq = tokf + (act ? tt : 0) * W::TOK * 4;
             float *rec = records ? ring_row + (long long)(cb + (act ? tt : 0)) * rp.stride : nullptr;
@@ -315,7 +321,7 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
                     if (i < sp.n_inter) {
                         short_put_tile<ST, K>(stage, r0, col, s);
                         __syncthreads();
-                        tile_store<ST, K, W::NT, kShortWarps, kShortSwizzle>(reinterpret_cast<ST *>(sp.inter) + (long long)m.slot * sp.s_slot +
+                        tile_store<ST, K, W::NT, kShortTileWarps, kShortSwizzle>(reinterpret_cast<ST *>(sp.inter) + (long long)m.slot * sp.s_slot +
                                                      (long long)i * sp.s_tok + (long long)h * sp.s_head +
                                                      us * P::CW,
                                                  V, stage);
@@ -335,36 +341,43 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
 }
 
 template <typename ST, int K, Mode MODE>
-__global__ void __launch_bounds__(WinShape<ST, K>::NT, kShortMinBlocks)
+__global__ void __launch_bounds__(WinShape<ST, K>::NT, WinShape<ST, K>::MINB)
     k_short(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len,
             const int nunits, const FastDiv hd, const FastDiv rd) {
     using P = ShortTile<ST, K>;
     using W = WinShape<ST, K>;
     extern __shared__ uint4 smem_short[];
     uint4 *stage0 = smem_short, *stage1 = smem_short + W::SC;
+    // descriptors of units i, i+1, i+2 (slot i % 3 holds unit i), computed by
+    // thread 0 two units ahead and published by the barrier that follows
+    __shared__ ShortMeta meta_s[3];
     const long long G = gridDim.x;
-    ShortMeta cur = short_meta<P::USL>(p, blockIdx.x, nunits, hd, rd);
-    short_issue<ST, K>(p, cur, max_len, stage0);
-    ShortMeta nxt = short_meta<P::USL>(p, (long long)blockIdx.x + G, nunits, hd, rd);
-    int sel = 0;
+    if (threadIdx.x == 0) {
+        meta_s[0] = short_meta<P::USL>(p, blockIdx.x, nunits, hd, rd);
+        meta_s[1] = short_meta<P::USL>(p, (long long)blockIdx.x + G, nunits, hd, rd);
+    }
+    __syncthreads();
+    short_issue<ST, K>(p, meta_s[0], max_len, stage0);
+    int sel = 0, mi = 0;
     for (long long u = blockIdx.x; u < nunits; u += G) {
         uint4 *s_cur = sel ? stage1 : stage0;
         uint4 *s_nxt = sel ? stage0 : stage1;
-        short_issue<ST, K>(p, nxt, max_len, s_nxt);
-        const ShortMeta later = short_meta<P::USL>(p, u + 2 * G, nunits, hd, rd);
+        const int m1 = mi == 2 ? 0 : mi + 1, m2 = m1 == 2 ? 0 : m1 + 1;
+        short_issue<ST, K>(p, meta_s[m1], max_len, s_nxt);
+        if (threadIdx.x == 0) meta_s[m2] = short_meta<P::USL>(p, u + 2 * G, nunits, hd, rd);
         cp_async_wait<1>();
         __syncthreads();
-        const bool commit = short_compute<ST, K, MODE>(p, rp, sp, max_len, cur, s_cur);
+        const bool commit = short_compute<ST, K, MODE>(p, rp, sp, max_len, meta_s[mi], s_cur);
         __syncthreads();
-        if (commit) {
-            tile_store<ST, K, W::NT, kShortWarps, kShortSwizzle>(reinterpret_cast<ST *>(p.state) + (long long)cur.slot * p.st_slot +
+        if (commit) {  // uniform over the CTA
+            const ShortMeta &cur = meta_s[mi];
+            tile_store<ST, K, W::NT, kShortTileWarps, kShortSwizzle>(reinterpret_cast<ST *>(p.state) + (long long)cur.slot * p.st_slot +
                                          (long long)cur.h * p.st_head + cur.us * P::CW,
                                      p.st_k, s_cur);
+            __syncthreads();  // the stage is refilled next iteration
         }
-        __syncthreads();
-        cur = nxt;
-        nxt = later;
         sel ^= 1;
+        mi = m1;
     }
     cp_async_wait<0>();
 }

@@ -71,9 +71,9 @@ def _load():
             vp, i32 = ctypes.c_void_p, ctypes.c_int
             for prec in ("f64", "f32"):
                 getattr(lib, f"oracle_fwd_{prec}").argtypes = [P, vp]
-                getattr(lib, f"oracle_verify_ring_{prec}").argtypes = [P, vp, vp, i32, i32, i32, vp]
+                getattr(lib, f"oracle_verify_ring_{prec}").argtypes = [P, vp, vp, i32, i32, i32, i32, vp]
                 getattr(lib, f"oracle_fwd_snapshots_{prec}").argtypes = [P, vp, vp, i32, i32]
-                getattr(lib, f"oracle_fold_{prec}").argtypes = [P, vp, i32, i32, i32, vp, vp]
+                getattr(lib, f"oracle_fold_{prec}").argtypes = [P, vp, i32, i32, i32, i32, vp, vp]
             lib.oracle_rollback.argtypes = [P, vp, i32, vp]
             lib.oracle_round_bf16.argtypes = [ctypes.c_double]
             lib.oracle_round_bf16.restype = ctypes.c_uint16
@@ -148,30 +148,32 @@ def fwd(p: Problem, work: str = "f64") -> np.ndarray:
 
 def verify_ring(p: Problem, ring: np.ndarray, ring_slot_idx, ring_len: int,
                 work: str = "f64") -> np.ndarray:
-    """Verify pass; writes records into ``ring`` [ring_rows, nk, ring_len, stride] float32."""
+    """Verify pass; writes records into ``ring`` [ring_rows, nk, ring_len, stride],
+    float32 or uint16 (bfloat16 bits, rounded to nearest-even)."""
     lib = _load()
-    assert ring.dtype == np.float32 and ring.flags.c_contiguous and ring.ndim == 4
+    assert ring.dtype in (np.float32, np.uint16) and ring.flags.c_contiguous and ring.ndim == 4
     assert ring.shape[1] == p.nk and ring.shape[2] == ring_len
     rsi = _c(ring_slot_idx, np.int32)
     out = p._out()
     s = p._c_struct()
     _check(getattr(lib, f"oracle_verify_ring_{work}")(
-        ctypes.byref(s), _ptr(out), _ptr(ring), ring.shape[0], ring_len, ring.shape[3],
-        _ptr(rsi)), "verify_ring")
+        ctypes.byref(s), _ptr(out), _ptr(ring), int(ring.dtype == np.uint16), ring.shape[0],
+        ring_len, ring.shape[3], _ptr(rsi)), "verify_ring")
     return out
 
 
 def fold(p: Problem, ring: np.ndarray, ring_slot_idx, counts, ring_len: int,
          work: str = "f64") -> None:
-    """Fold the first counts[b] records of each row into p.state in place."""
+    """Fold the first counts[b] records of each row into p.state in place; the ring
+    is float32 or uint16 (bfloat16 bits)."""
     lib = _load()
-    ring = _c(ring, np.float32)
+    ring = _c(ring, np.uint16 if ring.dtype == np.uint16 else np.float32)
     rsi = _c(ring_slot_idx, np.int32)
     cnt = _c(counts, np.int32)
     s = p._c_struct()
     _check(getattr(lib, f"oracle_fold_{work}")(
-        ctypes.byref(s), _ptr(ring), ring.shape[0], ring_len, ring.shape[3], _ptr(rsi),
-        _ptr(cnt)), "fold")
+        ctypes.byref(s), _ptr(ring), int(ring.dtype == np.uint16), ring.shape[0], ring_len,
+        ring.shape[3], _ptr(rsi), _ptr(cnt)), "fold")
 
 
 def fwd_snapshots(p: Problem, inter: np.ndarray, steps_per_token: int,

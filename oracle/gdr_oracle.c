@@ -43,10 +43,13 @@
  *   - eps = 1e-6 inside the square root (passed in);
  *   - a bf16 pool is widened exactly on load and rounded to nearest-even once
  *     per call at the end of the row;
- *   - ring record layout, in float32 elements:
- *       [ k^ (K) | alpha_0 .. alpha_{r-1}, zero-padded to a multiple of 4 |
+ *   - ring record layout, in elements of the ring's dtype (float32, or
+ *     bfloat16 rounded to nearest-even from the computed value):
+ *       [ k^ (K) | alpha_0 .. alpha_{r-1}, padded to a multiple of 8 |
  *         u_0 (V) | u_1 (V) | ... | u_{r-1} (V) ]
- *     where j = h mod r is the value head's position inside its key head;
+ *     where j = h mod r is the value head's position inside its key head
+ *     ("gated_delta_recurrence_verify_ring_gpu" Parameters: ring_dtype; only
+ *     a float32 ring keeps the fold bit-exact against the forward pass);
  *   - snapshot i is taken after step (i+1)*steps_per_token - 1 of the row;
  *     a partial trailing draft is not snapshotted.
  *
@@ -122,7 +125,7 @@ int oracle_ring_record_elements(int K, int V, int r)
 {
     if (K <= 0 || V <= 0 || r <= 0)
         return -1;
-    return K + ((r + 3) / 4) * 4 + r * V;
+    return K + ((r + 7) / 8) * 8 + r * V;
 }
 
 static int check_problem(const oracle_problem *p)

@@ -20,6 +20,13 @@ static void SFX(store_elem)(void *base, int bf16, size_t idx, REAL x)
         ((float *)base)[idx] = (float)x;
 }
 
+static REAL SFX(load_elem)(const void *base, int bf16, size_t idx)
+{
+    if (bf16)
+        return (REAL)bf16_bits_to_double(((const uint16_t *)base)[idx]);
+    return (REAL)((const float *)base)[idx];
+}
+
 /* One token of the recurrence for one (sequence, value head); S is [K][V].
  * "gated_delta_recurrence_fwd_gpu" summary (L2 normalisation, 1/sqrt(K) query
  * scale); "core.ssm.ops.gdp.fused_recurrent" Parameters (log decay g, beta).
@@ -74,7 +81,7 @@ static void SFX(token)(int K, int V, REAL *S, const float *q, const float *k,
  *   inter != NULL  : snapshots -- after every spt steps of a row the state is
  *                    stored at inter[slot, i, h] (i < n_inter).
  * out is [T, nv*V] in double; padding rows get exact zeros. */
-static int SFX(run)(const oracle_problem *p, double *out, float *ring, int ring_rows,
+static int SFX(run)(const oracle_problem *p, double *out, void *ring, int ring_bf16, int ring_rows,
                     int ring_len, int record_stride, const int32_t *ring_slot_idx,
                     void *inter, int n_inter, int spt)
 {
@@ -140,15 +147,15 @@ static int SFX(run)(const oracle_problem *p, double *out, float *ring, int ring_
                 for (int j = 0; j < V; ++j)
                     out[(size_t)t * value_dim + (size_t)h * V + j] = (double)o[j];
                 if (records) {
-                    float *rec = ring + (((size_t)rs * nk + hk) * ring_len + (size_t)(t - t0)) *
-                                            (size_t)record_stride;
+                    const size_t rec = (((size_t)rs * nk + hk) * ring_len + (size_t)(t - t0)) *
+                                       (size_t)record_stride;
                     if (jr == 0)
                         for (int i = 0; i < K; ++i)
-                            rec[i] = (float)kh[i];
-                    rec[K + jr] = (float)alpha;
-                    float *ur = rec + K + ((r + 3) / 4) * 4 + (size_t)jr * V;
+                            SFX(store_elem)(ring, ring_bf16, rec + i, kh[i]);
+                    SFX(store_elem)(ring, ring_bf16, rec + K + jr, alpha);
+                    const size_t ur = rec + K + ((r + 7) / 8) * 8 + (size_t)jr * V;
                     for (int j = 0; j < V; ++j)
-                        ur[j] = (float)u[j];
+                        SFX(store_elem)(ring, ring_bf16, ur + j, u[j]);
                 }
                 if (inter) {
                     const int64_t s = t - t0;
@@ -176,17 +183,18 @@ static int SFX(run)(const oracle_problem *p, double *out, float *ring, int ring_
  * written back in place ("gated_delta_recurrence_fwd_gpu", summary and Args). */
 int SFX(oracle_fwd)(const oracle_problem *p, double *out)
 {
-    return SFX(run)(p, out, NULL, 0, 0, 0, NULL, NULL, 0, 0);
+    return SFX(run)(p, out, NULL, 0, 0, 0, 0, NULL, NULL, 0, 0);
 }
 
-/* Verify pass ("gated_delta_recurrence_verify_ring_gpu", summary). */
-int SFX(oracle_verify_ring)(const oracle_problem *p, double *out, float *ring,
+/* Verify pass ("gated_delta_recurrence_verify_ring_gpu", summary); ring_bf16
+ * selects a bfloat16 ring (Parameters: ring_dtype). */
+int SFX(oracle_verify_ring)(const oracle_problem *p, double *out, void *ring, int ring_bf16,
                             int ring_rows, int ring_len, int record_stride,
                             const int32_t *ring_slot_idx)
 {
     if (!ring)
         return -1;
-    return SFX(run)(p, out, ring, ring_rows, ring_len, record_stride, ring_slot_idx,
+    return SFX(run)(p, out, ring, ring_bf16, ring_rows, ring_len, record_stride, ring_slot_idx,
                     NULL, 0, 0);
 }
 
@@ -198,7 +206,7 @@ int SFX(oracle_fwd_snapshots)(const oracle_problem *p, double *out, void *inter,
 {
     if (!inter)
         return -1;
-    return SFX(run)(p, out, NULL, 0, 0, 0, NULL, inter, n_inter, spt);
+    return SFX(run)(p, out, NULL, 0, 0, 0, 0, NULL, inter, n_inter, spt);
 }
 
 /* Fold: advance each live row's slot over its first counts[b] ring records.
@@ -207,7 +215,7 @@ int SFX(oracle_fwd_snapshots)(const oracle_problem *p, double *out, void *inter,
  * Each record applies S = alpha * S; S = S + k^ u^T -- the same two steps the
  * forward pass takes, so in float32 with a float32 ring the result is the
  * forward pass over the accepted prefix, bit for bit. */
-int SFX(oracle_fold)(const oracle_problem *p, const float *ring, int ring_rows,
+int SFX(oracle_fold)(const oracle_problem *p, const void *ring, int ring_bf16, int ring_rows,
                      int ring_len, int record_stride, const int32_t *ring_slot_idx,
                      const int32_t *counts)
 {
@@ -237,17 +245,18 @@ int SFX(oracle_fold)(const oracle_problem *p, const float *ring, int ring_rows,
             for (size_t e = 0; e < (size_t)K * V; ++e)
                 S[e] = SFX(load_state)(p, sbase + e);
             for (int t = 0; t < c; ++t) {
-                const float *rec =
-                    ring + (((size_t)rs * nk + hk) * ring_len + (size_t)t) * (size_t)record_stride;
-                const REAL alpha = (REAL)rec[K + jr];
-                const float *ur = rec + K + ((r + 3) / 4) * 4 + (size_t)jr * V;
+                const size_t rec =
+                    (((size_t)rs * nk + hk) * ring_len + (size_t)t) * (size_t)record_stride;
+                const REAL alpha = SFX(load_elem)(ring, ring_bf16, rec + K + jr);
+                const size_t ur = rec + K + ((r + 7) / 8) * 8 + (size_t)jr * V;
                 for (int i = 0; i < K; ++i)
                     for (int j = 0; j < V; ++j)
                         S[(size_t)i * V + j] = alpha * S[(size_t)i * V + j];
                 for (int i = 0; i < K; ++i)
                     for (int j = 0; j < V; ++j)
                         S[(size_t)i * V + j] =
-                            S[(size_t)i * V + j] + (REAL)rec[i] * (REAL)ur[j];
+                            S[(size_t)i * V + j] + SFX(load_elem)(ring, ring_bf16, rec + i) *
+                                                       SFX(load_elem)(ring, ring_bf16, ur + j);
             }
             for (size_t e = 0; e < (size_t)K * V; ++e)
                 SFX(store_elem)(p->state, p->state_bf16, sbase + e, S[e]);

@@ -48,10 +48,10 @@ def test_bf16_rounding_ties_to_even():
 
 
 def test_ring_record_elements():
-    # [k^ (K) | alpha x r padded to 4 | u x r (V each)]
-    assert oracle.ring_record_elements(128, 128, 2) == 128 + 4 + 256
-    assert oracle.ring_record_elements(16, 16, 1) == 16 + 4 + 16
-    assert oracle.ring_record_elements(64, 64, 5) == 64 + 8 + 320
+    # [k^ (K) | alpha x r padded to 8 | u x r (V each)]
+    assert oracle.ring_record_elements(128, 128, 2) == 128 + 8 + 256
+    assert oracle.ring_record_elements(16, 16, 1) == 16 + 8 + 16
+    assert oracle.ring_record_elements(64, 64, 9) == 64 + 16 + 576
 
 
 # ------------------------------------------------------ brute-force pins ---
@@ -345,9 +345,11 @@ def test_invalid_arguments_rejected():
 
 # ---------------------------------------------------------- verify / fold ---
 
-def _ring(w, nk, ring_len, rows):
+def _ring(w, nk, ring_len, rows, bf16=False):
     stride = oracle.ring_record_elements(w.K, w.V, w.nv // nk)
-    stride = (stride + 3) // 4 * 4
+    stride = (stride + 7) // 8 * 8
+    if bf16:  # 0x7FC0 is a bfloat16 NaN
+        return np.full((rows, nk, ring_len, stride), 0x7FC0, np.uint16)
     return np.full((rows, nk, ring_len, stride), np.nan, np.float32)
 
 
@@ -395,7 +397,7 @@ def test_verify_records_hold_normalised_key_alpha_and_correction():
         S = alpha * pool[slot, h].astype(np.float64)
         v = w.qkv[t, 2 * K + h * V: 2 * K + (h + 1) * V].astype(np.float64)
         u = float(w.beta[t, h]) * (v - S.T @ kh)
-        np.testing.assert_allclose(rec[K + 4 + h * V: K + 4 + (h + 1) * V], u, rtol=1e-6,
+        np.testing.assert_allclose(rec[K + 8 + h * V: K + 8 + (h + 1) * V], u, rtol=1e-6,
                                    atol=1e-7)
     assert np.isnan(ring[0, 0, 2:]).all()  # only two tokens recorded
 
@@ -407,11 +409,81 @@ def test_row_of_exactly_ring_len_records():
     pv = problem(w, state=pool.copy())
     oracle.verify_ring(pv, ring, np.array([0, 1], np.int32), 4)
     K, r = w.K, w.nv
-    fields = np.r_[0:K, K:K + r, K + 4:K + 4 + r * w.V]  # k^, alpha_j, u_j (not the pad)
+    fields = np.r_[0:K, K:K + r, K + 8:K + 8 + r * w.V]  # k^, alpha_j, u_j (not the pad)
     assert not np.isnan(ring[0][..., fields]).any()     # L == RING_LEN records
     assert np.isnan(ring[1]).all()              # L == RING_LEN + 1 commits instead
     assert (pv.state[w.slot_idx[0]] == pool[w.slot_idx[0]]).all()
     assert not (pv.state[w.slot_idx[1]] == pool[w.slot_idx[1]]).all()
+
+
+def test_bf16_ring_records_are_the_float32_records_rounded():
+    """A bfloat16 ring ("gated_delta_recurrence_verify_ring_gpu" Parameters:
+    ring_dtype) holds each record value rounded to nearest-even once: from the
+    float64 oracle's value, the bits equal rounding that value directly."""
+    w = _small(23, [3, 2], nk=2, nv=4, K=16, state_dtype="bf16", n_pad=1)
+    rsi = np.array([1, 0, 2], np.int32)
+    pool = w.state_pool()
+    r32 = _ring(w, w.nk, 4, 3)
+    r16 = _ring(w, w.nk, 4, 3, bf16=True)
+    # the float64 values behind the float32 ring: rerun the verify in float64 and
+    # compare bfloat16 bits with the float32 ring rounded from float64 where the
+    # float32 rounding cannot move a bfloat16 decision
+    out32 = oracle.verify_ring(problem(w, state=pool.copy()), r32, rsi, 4)
+    out16 = oracle.verify_ring(problem(w, state=pool.copy()), r16, rsi, 4)
+    assert (out32 == out16).all(), "the ring dtype does not change the output"
+    written = ~np.isnan(r32)
+    assert (written == (r16 != 0x7FC0)).all(), "same fields written"
+    wide = oracle.bf16_to_f64(r16[written])
+    ref = r32[written].astype(np.float64)
+    # bfloat16 keeps 8 significant bits: within half a bfloat16 ulp of the value
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 7)
+    assert (np.abs(wide - ref) <= ulp / 2 * (1 + 2 ** -16)).all()
+    # and on bfloat16-representable values the rounding is the identity
+    exact = oracle.round_bf16(wide)
+    assert (exact == r16[written]).all()
+
+
+def test_bf16_ring_fold_equals_float32_ring_fold_on_representable_records():
+    """Folding records whose values are bfloat16-representable gives the same
+    state from a float32 and from a bfloat16 ring: the fold only widens."""
+    w = _small(24, [1, 1, 1], nk=1, nv=2, K=16, state_dtype="f32")
+    stride = (oracle.ring_record_elements(16, 16, 2) + 7) // 8 * 8
+    rng = np.random.default_rng(25)
+    vals = rng.standard_normal((3, 1, 4, stride)) * 0.3
+    vals[..., 16:18] = rng.uniform(0.8, 1.0, (3, 1, 4, 2))
+    r16 = oracle.round_bf16(vals)
+    r32 = oracle.bf16_to_f64(r16).astype(np.float32)
+    counts = np.array([3, 0, 4], np.int32)
+    rsi = np.array([2, 0, 1], np.int32)
+    pool = w.state_pool()
+    p32, p16 = problem(w, state=pool.copy()), problem(w, state=pool.copy())
+    oracle.fold(p32, r32, rsi, counts, 4)
+    oracle.fold(p16, r16, rsi, counts, 4)
+    assert (p32.state == p16.state).all()
+    assert not (p32.state == pool).all()
+
+
+def test_bf16_ring_fold_tracks_the_forward_pass():
+    """verify + fold(c) with a bfloat16 ring stays within the records' rounding
+    of the forward pass over the first c tokens (not bit-exact: the pages keep
+    bit-exactness for float32 rings only)."""
+    w = _small(26, [5, 4], nk=1, nv=2, K=16, state_dtype="f32")
+    counts = np.array([3, 4], np.int32)
+    rsi = np.array([1, 0], np.int32)
+    pool = w.state_pool()
+    pv = problem(w, state=pool.copy())
+    ring = _ring(w, 1, 8, 2, bf16=True)
+    oracle.verify_ring(pv, ring, rsi, 8)
+    oracle.fold(pv, ring, rsi, counts, 8)
+    for b in range(w.batch):
+        s = int(w.slot_idx[b])
+        c = int(counts[b])
+        sub = dataclasses.replace(sub_workload(w, [b]), offsets=np.array([0, c], np.int32))
+        sub = dataclasses.replace(sub, qkv=sub.qkv[:c], decay=sub.decay[:c], beta=sub.beta[:c])
+        pf = problem(sub, state=pool.copy())
+        oracle.fwd(pf)
+        d = np.abs(pv.state[s].astype(np.float64) - pf.state[s])
+        assert d.max() < 2e-2 and d.max() > 0
 
 
 @pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
@@ -474,7 +546,8 @@ def test_fold_skips_zero_too_many_and_padding():
     w = dataclasses.replace(w, slot_idx=np.array([w.slot_idx[0], w.slot_idx[1], -1], np.int32))
     pool = w.state_pool()
     pv = problem(w, state=pool.copy())
-    ring = np.random.default_rng(0).standard_normal((3, 1, 4, 52)).astype(np.float32)
+    stride = oracle.ring_record_elements(16, 16, 2)
+    ring = np.random.default_rng(0).standard_normal((3, 1, 4, stride)).astype(np.float32)
     oracle.fold(pv, ring, np.array([0, 1, 2], np.int32), np.array([0, 5, 2], np.int32), 4)
     assert (pv.state == pool).all()
 

@@ -47,7 +47,8 @@ def parse():
     ap.add_argument("--impl", default="gdr", choices=["gdr", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "verify_fold", "gdp_snapshots"], default=None,
+    ap.add_argument("--only", choices=["prefill", "verify_fold", "verify_fold_bf16_ring", "gdp_snapshots"],
+                    default=None,
                     help="time just this secondary workload and print its figures (profiling aid)")
     ap.add_argument("--soak-s", type=float, default=1.0,
                     help="seconds of untimed steps after warm-up (steady clocks)")
@@ -283,16 +284,18 @@ def bench_prefill(dev, flush, stream, hbm_peak, steps):
     }
 
 
-def bench_verify_fold(dev, flush, stream, hbm_peak, steps):
-    """Speculative verify (bf16 pool, fp32 ring of RING_LEN 8) then fold."""
+def bench_verify_fold(dev, flush, stream, hbm_peak, steps, ring_dtype=None):
+    """Speculative verify (bf16 pool, fp32 or bf16 ring of RING_LEN 8) then fold."""
     import torch
     import gated_deltanet_linear_gdr_gb300 as gdr
     from gated_deltanet_linear_gdr_gb300 import workloads as W
     w = W.verify_fold()
     st = _pool_dev(w, dev)
     qkv, dec, bet, slot, off = (_to_dev(x, dev) for x in (w.qkv, w.decay, w.beta, w.slot_idx, w.offsets))
-    stride = (gdr.gdr_ring_record_elements(w.K, w.V, w.nv // w.nk) + 3) // 4 * 4
-    ring = torch.zeros((w.ring_rows, w.nk, w.ring_len, stride), device=dev)
+    ring_dtype = ring_dtype or torch.float32
+    stride = (gdr.gdr_ring_record_elements(w.K, w.V, w.nv // w.nk) + 7) // 8 * 8
+    ring = torch.zeros((w.ring_rows, w.nk, w.ring_len, stride), dtype=ring_dtype, device=dev)
+    rb = ring.element_size()
     rsi, cnt = _to_dev(w.ring_slot_idx, dev), _to_dev(w.counts, dev)
     out = torch.empty((w.total_tokens, w.nv * w.V), device=dev)
     # the caller of a verify window knows its longest row: the short-row kernel
@@ -307,14 +310,14 @@ def bench_verify_fold(dev, flush, stream, hbm_peak, steps):
     L = w.row_lengths
     short = L <= w.ring_len
     r = w.nv // w.nk
-    rec = w.K + ((r + 3) // 4) * 4 + r * w.V
+    rec = w.K + ((r + 7) // 8) * 8 + r * w.V
     conv = 2 * w.nk * w.K + w.nv * w.V
     vbytes = (w.batch * w.nv * w.K * w.V * 2 + int((~short).sum()) * w.nv * w.K * w.V * 2
               + w.total_tokens * (conv + 2 * w.nv + w.nv * w.V) * 4
-              + int(L[short].sum()) * w.nk * rec * 4)
+              + int(L[short].sum()) * w.nk * rec * rb)
     active = (w.counts > 0) & (w.counts <= w.ring_len) & (w.slot_idx >= 0)
     fbytes = (int(active.sum()) * w.nv * w.K * w.V * 2 * 2
-              + int(w.counts[active].sum()) * w.nk * rec * 4)
+              + int(w.counts[active].sum()) * w.nk * rec * rb)
     ht = w.live_head_tokens
     # roofline time of each kernel: the larger of its HBM time and its FMA-pipe time
     fp32_peak = fp32_fma_peak(dev)
@@ -323,7 +326,8 @@ def bench_verify_fold(dev, flush, stream, hbm_peak, steps):
                  fma_ops(int(w.counts[active].sum()) * w.nv, w.K, w.V, per=2) / fp32_peak)
     return {
         "workload": "verify: 127 rows x 5 drafts + 1 row of 12, RING_LEN 8, nk=16, nv=32, "
-                    "K=V=128, bf16 pool [256,32,128,128], fp32 ring [256,16,8,388]; then fold "
+                    f"K=V=128, bf16 pool [256,32,128,128], "
+                    f"{'bf16' if rb == 2 else 'fp32'} ring [256,16,8,{stride}]; then fold "
                     "of accepted counts ~U{0..5}",
         "verify_ms": tv, "fold_ms": tf, "head_tokens_per_s": ht / ((tv + tf) * 1e-3),
         "verify_hbm_gbs": vbytes / (tv * 1e-3) / 1e9, "fold_hbm_gbs": fbytes / (tf * 1e-3) / 1e9,
@@ -366,7 +370,14 @@ def bench_gdp_snapshots(dev, flush, stream, hbm_peak, steps):
     }
 
 
+def bench_verify_fold_bf16_ring(dev, flush, stream, hbm_peak, steps):
+    """The verify + fold workload with a bfloat16 ring (records rounded once)."""
+    import torch
+    return bench_verify_fold(dev, flush, stream, hbm_peak, steps, ring_dtype=torch.bfloat16)
+
+
 SECONDARY = {"prefill": bench_prefill, "verify_fold": bench_verify_fold,
+             "verify_fold_bf16_ring": bench_verify_fold_bf16_ring,
              "gdp_snapshots": bench_gdp_snapshots}
 
 

@@ -115,6 +115,10 @@ def _dev(t: torch.Tensor, name: str, dtype=None):
     return t
 
 
+def _ring_dtype(ring: torch.Tensor) -> int:
+    return GDR_BF16 if ring.dtype == torch.bfloat16 else GDR_F32
+
+
 def _state_dtype(state: torch.Tensor) -> int:
     if state.dtype == torch.bfloat16:
         return GDR_BF16
@@ -210,8 +214,8 @@ def gdr_fwd(qkv, decay, beta, state, slot_idx, offsets, out=None, *, decay_is_lo
 def gdr_verify_ring(qkv, decay, beta, state, slot_idx, offsets, ring, ring_slot_idx, out=None, *,
                     decay_is_log=False, use_qk_l2norm=True, scale=0.0, eps=1e-6, max_row_len=0):
     """Verify pass ("gated_delta_recurrence_verify_ring_gpu"); ring is
-    [ring_rows, nk, ring_len, record_stride] float32 (dense)."""
-    _dev(ring, "ring", torch.float32)
+    [ring_rows, nk, ring_len, record_stride] float32 or bfloat16 (dense)."""
+    _dev(ring, "ring", (torch.float32, torch.bfloat16))
     _dev(ring_slot_idx, "ring_slot_idx", torch.int32)
     if ring.dim() != 4 or not ring.is_contiguous():
         raise ValueError("ring must be a contiguous [ring_rows, nk, ring_len, record_stride] tensor")
@@ -223,7 +227,7 @@ def gdr_verify_ring(qkv, decay, beta, state, slot_idx, offsets, ring, ring_slot_
         raise ValueError("ring.shape[1] must equal nk")
     a = make_args(qkv, decay, beta, state, slot_idx, offsets, out, nk=nk, decay_is_log=decay_is_log,
                   use_qk_l2norm=use_qk_l2norm, scale=scale, eps=eps, max_row_len=max_row_len)
-    _check(load_library().gdr_verify_ring(ctypes.byref(a), ring.data_ptr(), GDR_F32, ring.shape[0],
+    _check(load_library().gdr_verify_ring(ctypes.byref(a), ring.data_ptr(), _ring_dtype(ring), ring.shape[0],
                                           ring.shape[2], ring.shape[3], ring_slot_idx.data_ptr(),
                                           _stream(qkv.device)))
     return out
@@ -231,13 +235,13 @@ def gdr_verify_ring(qkv, decay, beta, state, slot_idx, offsets, ring, ring_slot_
 
 def gdr_fold(state, slot_idx, ring, ring_slot_idx, counts):
     """Fold the first counts[b] records of each row into its slot (in place)."""
-    _dev(ring, "ring", torch.float32)
+    _dev(ring, "ring", (torch.float32, torch.bfloat16))
     _dev(ring_slot_idx, "ring_slot_idx", torch.int32)
     _dev(counts, "counts", torch.int32)
     if ring.dim() != 4 or not ring.is_contiguous():
         raise ValueError("ring must be a contiguous [ring_rows, nk, ring_len, record_stride] tensor")
     a = make_args(None, None, None, state, slot_idx, None, None, nk=ring.shape[1])
-    _check(load_library().gdr_fold(ctypes.byref(a), ring.data_ptr(), GDR_F32, ring.shape[0],
+    _check(load_library().gdr_fold(ctypes.byref(a), ring.data_ptr(), _ring_dtype(ring), ring.shape[0],
                                    ring.shape[2], ring.shape[3], ring_slot_idx.data_ptr(),
                                    counts.data_ptr(), _stream(state.device)))
 
@@ -323,14 +327,14 @@ def prepare_fwd(qkv, decay, beta, state, slot_idx, offsets, out, *, decay_is_log
 def prepare_verify_ring(qkv, decay, beta, state, slot_idx, offsets, ring, ring_slot_idx, out, *,
                         decay_is_log=False, use_qk_l2norm=True, scale=0.0, eps=1e-6,
                         max_row_len=0) -> Prepared:
-    _dev(ring, "ring", torch.float32)
+    _dev(ring, "ring", (torch.float32, torch.bfloat16))
     _dev(ring_slot_idx, "ring_slot_idx", torch.int32)
     if ring.dim() != 4 or not ring.is_contiguous():
         raise ValueError("ring must be a contiguous [ring_rows, nk, ring_len, record_stride] tensor")
     a = make_args(qkv, decay, beta, state, slot_idx, offsets, out, nk=_nk_from_qkv(qkv, state),
                   decay_is_log=decay_is_log, use_qk_l2norm=use_qk_l2norm, scale=scale, eps=eps,
                   max_row_len=max_row_len)
-    extra = (ring.data_ptr(), GDR_F32, ring.shape[0], ring.shape[2], ring.shape[3],
+    extra = (ring.data_ptr(), _ring_dtype(ring), ring.shape[0], ring.shape[2], ring.shape[3],
              ring_slot_idx.data_ptr())
     return Prepared(load_library().gdr_verify_ring, a, extra,
                     (qkv, decay, beta, state, slot_idx, offsets, out, ring, ring_slot_idx),
@@ -338,13 +342,13 @@ def prepare_verify_ring(qkv, decay, beta, state, slot_idx, offsets, ring, ring_s
 
 
 def prepare_fold(state, slot_idx, ring, ring_slot_idx, counts) -> Prepared:
-    _dev(ring, "ring", torch.float32)
+    _dev(ring, "ring", (torch.float32, torch.bfloat16))
     _dev(ring_slot_idx, "ring_slot_idx", torch.int32)
     _dev(counts, "counts", torch.int32)
     if ring.dim() != 4 or not ring.is_contiguous():
         raise ValueError("ring must be a contiguous [ring_rows, nk, ring_len, record_stride] tensor")
     a = make_args(None, None, None, state, slot_idx, None, None, nk=ring.shape[1])
-    extra = (ring.data_ptr(), GDR_F32, ring.shape[0], ring.shape[2], ring.shape[3],
+    extra = (ring.data_ptr(), _ring_dtype(ring), ring.shape[0], ring.shape[2], ring.shape[3],
              ring_slot_idx.data_ptr(), counts.data_ptr())
     return Prepared(load_library().gdr_fold, a, extra,
                     (state, slot_idx, ring, ring_slot_idx, counts), state.device)

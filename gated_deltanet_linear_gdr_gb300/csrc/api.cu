@@ -164,19 +164,25 @@ int launched(cudaError_t e, const char *fn) {
     return ok();
 }
 
+// Ring checks; writers (the verify pass) need a 16-byte aligned ring, the fold
+// reads any element-aligned ring.
 int check_ring(int32_t ring_dtype, int64_t ring_rows, int32_t ring_len, int64_t record_stride,
                const void *ring, const int32_t *ring_slot_idx, int K, int V, int r, int batch,
-               const char *fn) {
-    if (ring_dtype != GDR_F32)
-        return fail(GDR_ERR_UNSUPPORTED, "%s: ring_dtype must be GDR_F32", fn);
+               bool writer, const char *fn) {
+    if (ring_dtype != GDR_F32 && ring_dtype != GDR_BF16)
+        return fail(GDR_ERR_UNSUPPORTED, "%s: ring_dtype %d (GDR_F32 or GDR_BF16)", fn, ring_dtype);
     if (ring_len < 1 || ring_len > 32)
         return fail(GDR_ERR_UNSUPPORTED, "%s: ring_len %d not in [1, 32]", fn, ring_len);
     const int need = gdr_ring_record_elements(K, V, r);
-    if (record_stride < need || record_stride % 4)
-        return fail(GDR_ERR_INVALID_ARG, "%s: record_stride %lld must be a multiple of 4 and >= %d", fn,
-                    (long long)record_stride, need);
+    const int mult = ring_dtype == GDR_BF16 ? 8 : 4;  // records start on 16 bytes
+    if (record_stride < need || record_stride % mult)
+        return fail(GDR_ERR_INVALID_ARG, "%s: record_stride %lld must be a multiple of %d and >= %d", fn,
+                    (long long)record_stride, mult, need);
     if (batch > 0 && (!ring || !ring_slot_idx || ring_rows <= 0))
         return fail(GDR_ERR_INVALID_ARG, "%s: ring/ring_slot_idx NULL or ring_rows <= 0", fn);
+    const uintptr_t align = writer ? 16 : (ring_dtype == GDR_BF16 ? 2 : 4);
+    if (batch > 0 && (reinterpret_cast<uintptr_t>(ring) % align))
+        return fail(GDR_ERR_UNSUPPORTED, "%s: ring must be %d-byte aligned", fn, (int)align);
     return GDR_OK;
 }
 
@@ -212,7 +218,7 @@ int gdr_output_shape(int64_t total_tokens, int32_t nv, int32_t V, int64_t out_sh
 int gdr_ring_record_elements(int32_t K, int32_t V, int32_t ratio) {
     if (K <= 0 || V <= 0 || ratio <= 0)
         return fail(GDR_ERR_INVALID_ARG, "gdr_ring_record_elements: invalid arguments");
-    return K + ((ratio + 3) / 4) * 4 + ratio * V;
+    return K + ((ratio + 7) / 8) * 8 + ratio * V;
 }
 
 int gdr_fwd(const gdr_step_args *a, void *stream) {
@@ -227,13 +233,13 @@ int gdr_fwd(const gdr_step_args *a, void *stream) {
     return launched(launch_rows(p, a, gdr::Mode::Fwd, gdr::RingParams{}, gdr::SnapParams{}, s), "gdr_fwd");
 }
 
-int gdr_verify_ring(const gdr_step_args *a, float *ring, int32_t ring_dtype, int64_t ring_rows,
+int gdr_verify_ring(const gdr_step_args *a, void *ring, int32_t ring_dtype, int64_t ring_rows,
                     int32_t ring_len, int64_t record_stride, const int32_t *ring_slot_idx, void *stream) {
     int rc = check_step(a, "gdr_verify_ring");
     if (rc) return rc;
     const int r = a->nv / a->nk;
     rc = check_ring(ring_dtype, ring_rows, ring_len, record_stride, ring, ring_slot_idx, a->K, a->V, r,
-                    a->batch, "gdr_verify_ring");
+                    a->batch, true, "gdr_verify_ring");
     if (rc) return rc;
     if (a->batch == 0) return ok();
     unsigned *st = nullptr;
@@ -241,23 +247,24 @@ int gdr_verify_ring(const gdr_step_args *a, float *ring, int32_t ring_dtype, int
     const gdr::StepParams p = lower(a, st);
     gdr::RingParams rp{};
     rp.ring = ring;
+    rp.bf16 = ring_dtype == GDR_BF16;
     rp.rows = ring_rows;
     rp.len = ring_len;
     rp.stride = record_stride;
     rp.ring_slot = ring_slot_idx;
     rp.alpha_off = a->K;
-    rp.u_off = a->K + ((r + 3) / 4) * 4;
+    rp.u_off = a->K + ((r + 7) / 8) * 8;
     return launched(launch_rows(p, a, gdr::Mode::Verify, rp, gdr::SnapParams{}, static_cast<cudaStream_t>(stream)),
                     "gdr_verify_ring");
 }
 
-int gdr_fold(const gdr_step_args *a, const float *ring, int32_t ring_dtype, int64_t ring_rows, int32_t ring_len,
+int gdr_fold(const gdr_step_args *a, const void *ring, int32_t ring_dtype, int64_t ring_rows, int32_t ring_len,
              int64_t record_stride, const int32_t *ring_slot_idx, const int32_t *counts, void *stream) {
     int rc = check_pool(a, "gdr_fold");
     if (rc) return rc;
     const int r = a->nv / a->nk;
     rc = check_ring(ring_dtype, ring_rows, ring_len, record_stride, ring, ring_slot_idx, a->K, a->V, r,
-                    a->batch, "gdr_fold");
+                    a->batch, false, "gdr_fold");
     if (rc) return rc;
     if (a->batch == 0) return ok();
     if (!counts) return fail(GDR_ERR_INVALID_ARG, "gdr_fold: counts is NULL");
@@ -275,13 +282,14 @@ int gdr_fold(const gdr_step_args *a, const float *ring, int32_t ring_dtype, int6
     p.max_slots = a->max_slots;
     p.slot_idx = a->slot_idx;
     p.ring = ring;
+    p.ring_bf16 = ring_dtype == GDR_BF16;
     p.ring_rows = ring_rows;
     p.ring_len = ring_len;
     p.stride = record_stride;
     p.ring_slot = ring_slot_idx;
     p.counts = counts;
     p.alpha_off = a->K;
-    p.u_off = a->K + ((r + 3) / 4) * 4;
+    p.u_off = a->K + ((r + 7) / 8) * 8;
     p.status = st;
     return launched(gdr::launch_fold(p, a->K, a->state_dtype == GDR_BF16, static_cast<cudaStream_t>(stream)),
                     "gdr_fold");

@@ -107,6 +107,33 @@ __device__ __forceinline__ void store_f32(float *p, long long stride, bool vec, 
     for (int i = 0; i < N; ++i) p[i * stride] = x[i];
 }
 
+// ---- ring records: float32, or bfloat16 rounded to nearest-even once --------
+// i is an element index into the ring; i2 is even, i4 a multiple of 4 (the
+// ring base is 16-byte aligned and record strides keep the alignment).
+__device__ __forceinline__ void ring_put1(void *ring, int bf16, long long i, float v) {
+    if (bf16)
+        reinterpret_cast<uint16_t *>(ring)[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    else
+        reinterpret_cast<float *>(ring)[i] = v;
+}
+__device__ __forceinline__ void ring_put2(void *ring, int bf16, long long i2, float a, float b) {
+    if (bf16)
+        *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<uint16_t *>(ring) + i2) = __floats2bfloat162_rn(a, b);
+    else
+        *reinterpret_cast<float2 *>(reinterpret_cast<float *>(ring) + i2) = make_float2(a, b);
+}
+__device__ __forceinline__ void ring_put4(void *ring, int bf16, long long i4, float4 v) {
+    if (bf16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+        uint2 w;
+        w.x = *reinterpret_cast<const uint32_t *>(&lo);
+        w.y = *reinterpret_cast<const uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(ring) + i4) = w;
+    } else {
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(ring) + i4) = v;
+    }
+}
+
 // ---- the fixed per-token arithmetic ----------------------------------------
 
 __device__ __forceinline__ float chain_first(float x, float y) { return __fmul_rn(x, y); }

@@ -31,15 +31,17 @@ struct StepParams {
     unsigned *status;
 };
 
-// Verify ring ("gated_delta_recurrence_verify_ring_gpu", ring / ring_slot_idx).
+// Verify ring ("gated_delta_recurrence_verify_ring_gpu", ring / ring_slot_idx /
+// ring_dtype): float32 records, or bfloat16 (bf16 != 0).
 struct RingParams {
-    float *ring;
+    void *ring;        // 16-byte aligned
+    int bf16;
     long long rows;
     int len;
     long long stride;  // elements per record
     const int *ring_slot;
     int alpha_off;     // = K
-    int u_off;         // = K + 4*ceil(r/4)
+    int u_off;         // = K + 8*ceil(r/8)
 };
 
 // Snapshots ("core.ssm.ops.gdp.fused_recurrent", intermediate_states).
@@ -56,7 +58,8 @@ struct FoldParams {
     long long st_slot, st_head, st_k;
     long long max_slots;
     const int *slot_idx;
-    const float *ring;
+    const void *ring;
+    int ring_bf16;
     long long ring_rows;
     int ring_len;
     long long stride;

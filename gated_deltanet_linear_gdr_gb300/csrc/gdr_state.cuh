@@ -258,11 +258,12 @@ template <int RG, int C> struct LaneState<RG, C, false> {
 // rows back pair-interleaved).  Every lane of the warp must call this
 // together (shuffles); lanes with act == false contribute zeros and write
 // nothing.  Writes k^ = k * inv_k and q~ = q * inv_q * scale in vpos order,
-// and, from lane gl == 0, *kq_out = k^ . q~.  ring_k (if not null) receives
-// k^ in natural order.
+// and, from lane gl == 0, *kq_out = k^ . q~.  When ring is not null, k^ is
+// also written in natural order to elements ring_k .. ring_k + K - 1 of the
+// ring (float32, or bfloat16 when ring_bf16).
 template <int K, bool RPAIR, int PADROWS>
 __device__ __forceinline__ void norm_token(float *q, float *k, float *kq_out, int gl, bool act, const StepParams &p,
-                                           float *ring_k) {
+                                           void *ring, int ring_bf16, long long ring_k) {
     constexpr int GPL = RPAIR ? 2 : 1, NL = K / 8 / GPL, NR = 8 * GPL;
     static_assert(PADROWS % NR == 0, "a lane's rows must not straddle padding");
     const int r0 = gl * NR;
@@ -312,10 +313,10 @@ __device__ __forceinline__ void norm_token(float *q, float *k, float *kq_out, in
         *reinterpret_cast<float4 *>(k + o + m) = make_float4(kn[rr[0]], kn[rr[1]], kn[rr[2]], kn[rr[3]]);
         *reinterpret_cast<float4 *>(q + o + m) = make_float4(qn[rr[0]], qn[rr[1]], qn[rr[2]], qn[rr[3]]);
     }
-    if (ring_k) {
+    if (ring) {
 #pragma unroll
         for (int m = 0; m < NR; m += 4)
-            *reinterpret_cast<float4 *>(ring_k + r0 + m) = make_float4(kn[m], kn[m + 1], kn[m + 2], kn[m + 3]);
+            ring_put4(ring, ring_bf16, ring_k + r0 + m, make_float4(kn[m], kn[m + 1], kn[m + 2], kn[m + 3]));
     }
     if (gl == 0) *kq_out = kq;
 }

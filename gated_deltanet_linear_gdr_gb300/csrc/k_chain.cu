@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT, 4)
 
     // Verify: rows of at most ring_len tokens record; longer rows commit.
     bool records = false, commit = true;
-    float *ring_row = nullptr;
+    long long ring_row = 0;  // element index of this (ring row, key head)'s first record
     const int hk = h / p.r, jr = h % p.r;
     if constexpr (MODE == Mode::Verify) {
         if (L <= rp.len) {
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT, 4)
                 if (leader) flag(p.status, GDR_STATUS_BAD_RING_SLOT);
             } else {
                 records = true;
-                ring_row = rp.ring + ((long long)rs * p.nk + hk) * rp.len * rp.stride;
+                ring_row = ((long long)rs * p.nk + hk) * rp.len * rp.stride;
             }
         }
     }
@@ -186,12 +186,13 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT, 4)
             const int tt = tb + warp + W * (lane / NL);
             const bool act = tt < tc;
             const int ts = act ? tt : 0;
-            float *rec = records ? ring_row + (long long)(cb + ts) * rp.stride : nullptr;
-            norm_token<K, Sh::RPAIR, ROWS>(qb[ts], kb[ts], &sb[ts][2], lane % NL, act, p, rec_k ? rec : nullptr);
+            const long long rec = ring_row + (long long)(cb + ts) * rp.stride;
+            norm_token<K, Sh::RPAIR, ROWS>(qb[ts], kb[ts], &sb[ts][2], lane % NL, act, p,
+                                           rec_k ? rp.ring : nullptr, rp.bf16, rec);
             if (act && lane % NL == 0) {
                 const float alpha = gdr_alpha(sb[ts][0], p.decay_is_log);
                 sb[ts][0] = alpha;
-                if (rec_alpha) rec[rp.alpha_off + jr] = alpha;
+                if (rec_alpha) ring_put1(rp.ring, rp.bf16, rec + rp.alpha_off + jr, alpha);
             }
         }
         __syncthreads();
@@ -216,9 +217,14 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT, 4)
             if (kl == 0) store_f32<C>(obase + (long long)step * p.out_ss, p.out_vs, p.out_vec, o);
             if constexpr (MODE == Mode::Verify) {
                 if (records && kl == 0) {
-                    float *rec = ring_row + (long long)step * rp.stride + rp.u_off + jr * V + col0;
+                    const long long rec = ring_row + (long long)step * rp.stride + rp.u_off + jr * V + col0;
+                    if constexpr (C % 2 == 0) {
 #pragma unroll
-                    for (int c = 0; c < C; ++c) rec[c] = u[c];
+                        for (int c = 0; c < C; c += 2) ring_put2(rp.ring, rp.bf16, rec + c, u[c], u[c + 1]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < C; ++c) ring_put1(rp.ring, rp.bf16, rec + c, u[c]);
+                    }
                 }
             }
             // One sweep: S <- k^_t u^T + alpha S, and token t+1's partials on the new S

@@ -7,7 +7,8 @@
 // the records the verify pass wrote, then the state is written back once.  The
 // advance is the same float32 operation the forward pass applies, so with a
 // float32 ring the result is the forward pass over the accepted prefix, bit for
-// bit.
+// bit; a bfloat16 ring (records rounded once by the verify pass) is widened
+// exactly.  Both kernels are templated on the ring's element type RT.
 //
 // Rollback ("core.ssm.ops.gdp.fused_recurrent", intermediate_states): a copy of
 // the accepted draft's snapshot over the live state.
@@ -28,7 +29,36 @@ template <typename ST, int K> struct FoldShape {
     static constexpr int BLOCKS = K / RB < 1 ? 1 : K / RB;         // CTAs per (row, head)
 };
 
-template <typename ST, int K>
+// Ring element i widened to float32.
+template <typename RT> __device__ __forceinline__ float ring_get(const void *ring, long long i) {
+    return to_f32(reinterpret_cast<const RT *>(ring)[i]);
+}
+
+// N consecutive ring elements from shared memory (p 16-byte aligned when N % 4 == 0), widened.
+template <typename RT, int N>
+__device__ __forceinline__ void ring_vec(const RT *p, float (&o)[N]) {
+    if constexpr (N % 4 == 0 && sizeof(RT) == 4) {
+#pragma unroll
+        for (int i = 0; i < N; i += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(p + i);
+            o[i] = a.x; o[i + 1] = a.y; o[i + 2] = a.z; o[i + 3] = a.w;
+        }
+    } else if constexpr (N % 4 == 0 && sizeof(RT) == 2) {
+#pragma unroll
+        for (int i = 0; i < N; i += 4) {
+            const uint2 a = *reinterpret_cast<const uint2 *>(p + i);
+            o[i] = __uint_as_float(a.x << 16);
+            o[i + 1] = __uint_as_float(a.x & 0xffff0000u);
+            o[i + 2] = __uint_as_float(a.y << 16);
+            o[i + 3] = __uint_as_float(a.y & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) o[i] = to_f32(p[i]);
+    }
+}
+
+template <typename ST, int K, typename RT>
 __global__ void __launch_bounds__(kFoldThreads) k_fold(const FoldParams p) {
     using Sh = FoldShape<ST, K>;
     constexpr int V = K, CF = Sh::CF, LVF = Sh::LVF, RPP = Sh::RPP, RF = Sh::RF, RB = Sh::RB;
@@ -62,16 +92,17 @@ __global__ void __launch_bounds__(kFoldThreads) k_fold(const FoldParams p) {
         return;
     }
     const int hk = h / p.r, jr = h % p.r;
-    const float *rrow = p.ring + ((long long)rs * p.nk + hk) * p.ring_len * p.stride;
+    const long long rrow = ((long long)rs * p.nk + hk) * p.ring_len * p.stride;
     for (int idx = tid; idx < c * K; idx += kFoldThreads) {
         const int t = idx / K, i = idx - t * K;
-        kh_s[t][i] = rrow[(long long)t * p.stride + i];
+        kh_s[t][i] = ring_get<RT>(p.ring, rrow + (long long)t * p.stride + i);
     }
     for (int idx = tid; idx < c * V; idx += kFoldThreads) {
         const int t = idx / V, j = idx - t * V;
-        u_s[t][j] = rrow[(long long)t * p.stride + p.u_off + jr * V + j];
+        u_s[t][j] = ring_get<RT>(p.ring, rrow + (long long)t * p.stride + p.u_off + jr * V + j);
     }
-    for (int t = tid; t < c; t += kFoldThreads) a_s[t] = rrow[(long long)t * p.stride + p.alpha_off + jr];
+    for (int t = tid; t < c; t += kFoldThreads)
+        a_s[t] = ring_get<RT>(p.ring, rrow + (long long)t * p.stride + p.alpha_off + jr);
     __syncthreads();
 
     const int lv = tid % LVF, rsub = tid / LVF;
@@ -150,7 +181,7 @@ __global__ void __launch_bounds__(kFoldThreads) k_rollback(const RollbackParams 
 // columns (t % LV) * C .. + C - 1, so a warp's loads and stores cover whole
 // rows.
 
-template <typename ST, int K, int NTT> struct FoldTile {
+template <typename ST, int K, int NTT, typename RT = float> struct FoldTile {
     static constexpr int V = K;
     static constexpr int NT = NTT;                                  // threads per CTA
     static constexpr int C = 16 / (int)sizeof(ST);                  // columns per thread
@@ -159,7 +190,9 @@ template <typename ST, int K, int NTT> struct FoldTile {
     static constexpr int KT = cmin(K, 16384 / (V * (int)sizeof(ST)));  // rows per unit
     static constexpr int R = KT / LKR;                              // rows per thread
     static constexpr int KS = K / KT;                               // units per (row, head)
-    static constexpr int RQ = KT / 4 + V / 4 + 1;                   // 16-byte chunks per staged record
+    static constexpr int EPR = 16 / (int)sizeof(RT);                // ring elements per 16-byte chunk
+    static constexpr int RK = KT / EPR, RU = V / EPR;               // chunks of the k^ slice and of u
+    static constexpr int RQ = RK + RU + 1;                          // + the chunk holding alpha
     static constexpr bool OK = LV <= NT && R >= 1 && K % KT == 0;
 };
 
@@ -170,9 +203,9 @@ template <typename ST, int K, int NTT> struct FoldTile {
 // per SM keep enough loads in flight without a software pipeline.
 constexpr int kFoldDirectThreads = 256;
 
-template <typename ST, int K>
+template <typename ST, int K, typename RT>
 __global__ void __launch_bounds__(kFoldDirectThreads) k_fold_direct(const FoldParams p) {
-    using F = FoldTile<ST, K, kFoldDirectThreads>;
+    using F = FoldTile<ST, K, kFoldDirectThreads, RT>;
     constexpr int C = F::C, R = F::R;
     using VT = typename Pack<ST, C>::VT;
     extern __shared__ uint4 smem_fd[];
@@ -203,20 +236,19 @@ __global__ void __launch_bounds__(kFoldDirectThreads) k_fold_direct(const FoldPa
     VT raw[R];
 #pragma unroll
     for (int i = 0; i < R; ++i) raw[i] = *reinterpret_cast<const VT *>(rows + (long long)i * p.st_k);
-    // records -> shared memory: per record RQ chunks [k^ slice | u | alpha]
+    // records -> shared memory: per record RQ chunks [k^ slice | u | the chunk holding alpha]
     const int jr = h % p.r;
     {
         const int hk = h / p.r;
-        const float *rrow = p.ring + ((long long)rs * p.nk + hk) * p.ring_len * p.stride;
-        constexpr int RV = F::KT / 4 + K / 4;
-        for (int ch = tid; ch < c * RV; ch += F::NT) {
-            const int t = ch / RV, r = ch - t * RV;
-            const float *rec = rrow + (long long)t * p.stride;
-            const float *g = r < F::KT / 4 ? rec + ks * F::KT + 4 * r : rec + p.u_off + jr * K + 4 * (r - F::KT / 4);
-            cp_async16(smem_fd + t * F::RQ + r, g);
+        const RT *rrow = reinterpret_cast<const RT *>(p.ring) + ((long long)rs * p.nk + hk) * p.ring_len * p.stride;
+        const int a0 = p.alpha_off + (jr / F::EPR) * F::EPR;  // alpha_off is a multiple of 8
+        for (int ch = tid; ch < c * F::RQ; ch += F::NT) {
+            const int t = ch / F::RQ, r = ch - t * F::RQ;
+            const RT *rec = rrow + (long long)t * p.stride;
+            const RT *g = r < F::RK ? rec + ks * F::KT + F::EPR * r
+                                    : (r < F::RK + F::RU ? rec + p.u_off + jr * K + F::EPR * (r - F::RK) : rec + a0);
+            cp_async16(smem_fd + ch, g);
         }
-        for (int t = tid; t < c; t += F::NT)
-            cp_async4(smem_fd + t * F::RQ + RV, rrow + (long long)t * p.stride + p.alpha_off + jr);
         cp_async_commit();
         cp_async_wait<0>();
         __syncthreads();
@@ -229,26 +261,13 @@ __global__ void __launch_bounds__(kFoldDirectThreads) k_fold_direct(const FoldPa
 #pragma unroll
         for (int cc = 0; cc < C; ++cc) s[i][cc] = x.get(cc);
     }
-    const float *recs = reinterpret_cast<const float *>(smem_fd);
+    const RT *recs = reinterpret_cast<const RT *>(smem_fd);
     for (int t = 0; t < c; ++t) {
-        const float *rec = recs + t * F::RQ * 4;
-        const float alpha = rec[F::KT + K];
+        const RT *rec = recs + t * F::RQ * F::EPR;
+        const float alpha = to_f32(rec[(F::RK + F::RU) * F::EPR + jr % F::EPR]);
         float kh[R], uu[C];
-        if constexpr (R % 4 == 0) {
-#pragma unroll
-            for (int i = 0; i < R; i += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(rec + r0 + i);
-                kh[i] = a4.x; kh[i + 1] = a4.y; kh[i + 2] = a4.z; kh[i + 3] = a4.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < R; ++i) kh[i] = rec[r0 + i];
-        }
-#pragma unroll
-        for (int cc = 0; cc < C; cc += 4) {
-            const float4 b4 = *reinterpret_cast<const float4 *>(rec + F::KT + cg * C + cc);
-            uu[cc] = b4.x; uu[cc + 1] = b4.y; uu[cc + 2] = b4.z; uu[cc + 3] = b4.w;
-        }
+        ring_vec<RT, R>(rec + r0, kh);
+        ring_vec<RT, C>(rec + F::KT + cg * C, uu);
 #pragma unroll
         for (int i = 0; i < R; ++i) advance_cols<C>(s[i], kh[i], uu, alpha);
     }
@@ -256,18 +275,18 @@ __global__ void __launch_bounds__(kFoldDirectThreads) k_fold_direct(const FoldPa
     for (int i = 0; i < R; ++i) pack_store<ST, C>(reinterpret_cast<uint4 *>(rows + (long long)i * p.st_k), s[i]);
 }
 
-template <typename ST, int K> static cudaError_t launch_fold_direct_t(const FoldParams &p, cudaStream_t st) {
-    using F = FoldTile<ST, K, kFoldDirectThreads>;
+template <typename ST, int K, typename RT> static cudaError_t launch_fold_direct_t(const FoldParams &p, cudaStream_t st) {
+    using F = FoldTile<ST, K, kFoldDirectThreads, RT>;
     const int smem = p.ring_len * F::RQ * 16;
     const long long blocks = (long long)p.batch * p.nv * F::KS;
-    if (blocks > 0) k_fold_direct<ST, K><<<(unsigned)blocks, F::NT, smem, st>>>(p);
+    if (blocks > 0) k_fold_direct<ST, K, RT><<<(unsigned)blocks, F::NT, smem, st>>>(p);
     return cudaGetLastError();
 }
 
-template <typename ST, int K> static cudaError_t launch_fold_t(const FoldParams &p, cudaStream_t st) {
+template <typename ST, int K, typename RT> static cudaError_t launch_fold_t(const FoldParams &p, cudaStream_t st) {
     const long long blocks = (long long)p.batch * p.nv * FoldShape<ST, K>::BLOCKS;
     const size_t smem = (size_t)p.ring_len * (2 * K + 1) * sizeof(float);  // <= 32 x 257 x 4 bytes
-    if (blocks > 0) k_fold<ST, K><<<(unsigned)blocks, kFoldThreads, smem, st>>>(p);
+    if (blocks > 0) k_fold<ST, K, RT><<<(unsigned)blocks, kFoldThreads, smem, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -277,14 +296,18 @@ template <typename ST, int K> static cudaError_t launch_rollback_t(const Rollbac
     return cudaGetLastError();
 }
 
-template <typename ST, int K> static cudaError_t launch_fold_any(const FoldParams &p, cudaStream_t s) {
-    const bool aligned = (reinterpret_cast<uintptr_t>(p.ring) & 15u) == 0 && p.stride % 4 == 0 &&
-                         p.u_off % 4 == 0;
-    if constexpr (FoldTile<ST, K, kFoldDirectThreads>::OK) {
-        if (aligned && (long long)p.batch * p.nv * FoldTile<ST, K, kFoldDirectThreads>::KS < (1ll << 31))
-            return launch_fold_direct_t<ST, K>(p, s);
+template <typename ST, int K, typename RT> static cudaError_t launch_fold_rt(const FoldParams &p, cudaStream_t s) {
+    using F = FoldTile<ST, K, kFoldDirectThreads, RT>;
+    const bool aligned = (reinterpret_cast<uintptr_t>(p.ring) & 15u) == 0 && p.stride % F::EPR == 0 &&
+                         p.u_off % F::EPR == 0 && p.alpha_off % 8 == 0;
+    if constexpr (F::OK) {
+        if (aligned && (long long)p.batch * p.nv * F::KS < (1ll << 31)) return launch_fold_direct_t<ST, K, RT>(p, s);
     }
-    return launch_fold_t<ST, K>(p, s);
+    return launch_fold_t<ST, K, RT>(p, s);
+}
+
+template <typename ST, int K> static cudaError_t launch_fold_any(const FoldParams &p, cudaStream_t s) {
+    return p.ring_bf16 ? launch_fold_rt<ST, K, uint16_t>(p, s) : launch_fold_rt<ST, K, float>(p, s);
 }
 
 cudaError_t launch_fold(const FoldParams &p, int K, bool bf16, cudaStream_t s) {

@@ -235,7 +235,7 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
     }
     // Verify: rows of at most ring_len tokens record and leave the pool alone.
     bool records = false, commit = true;
-    float *ring_row = nullptr;
+    long long ring_row = 0;  // element index of this (ring row, key head)'s first record
     if constexpr (MODE == Mode::Verify) {
         if (L <= rp.len) {
             commit = false;
@@ -244,7 +244,7 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
                 if (leader) flag(p.status, GDR_STATUS_BAD_RING_SLOT);
             } else {
                 records = true;
-                ring_row = rp.ring + ((long long)rs * p.nk + m.hk) * rp.len * rp.stride;
+                ring_row = ((long long)rs * p.nk + m.hk) * rp.len * rp.stride;
             }
         }
     }
@@ -256,7 +256,7 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
     bool overflow = false;
     // lanes kl == 0 write the output (and u records) of their C columns
     const bool w_out = kl == 0;
-    float *uptr = records ? ring_row + rp.u_off + jr * V + us * P::CW + col : nullptr;
+    long long uidx = ring_row + rp.u_off + jr * V + us * P::CW + col;  // this lane's u record
     const bool rec_alpha = records && us == 0;
     const bool rec_k = rec_alpha && jr == 0;
 
@@ -276,13 +276,14 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
             const int tt = tb + TPW * warp + lane / NL;
             const bool act = tt < tc;
             float *tq = tokf + (act ? tt : 0) * W::TOK * 4;
-            float *rec = records ? ring_row + (long long)(cb + (act ? tt : 0)) * rp.stride : nullptr;
+            const long long rec = ring_row + (long long)(cb + (act ? tt : 0)) * rp.stride;
             float *ab = tq + W::TOKV * 4;
-            norm_token<K, true, ROWS>(tq, tq + W::KP, ab + 2, lane % NL, act, p, rec_k ? rec : nullptr);
+            norm_token<K, true, ROWS>(tq, tq + W::KP, ab + 2, lane % NL, act, p, rec_k ? rp.ring : nullptr, rp.bf16,
+                                      rec);
             if (act && lane % NL == 0) {
                 const float alpha = gdr_alpha(ab[0], p.decay_is_log);
                 ab[0] = alpha;
-                if (rec_alpha) rec[rp.alpha_off + jr] = alpha;
+                if (rec_alpha) ring_put1(rp.ring, rp.bf16, rec + rp.alpha_off + jr, alpha);
             }
         }
         __syncthreads();
@@ -307,12 +308,12 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
             if (w_out) {
                 store_f32<C>(optr, p.out_vs, p.out_vec, o);
                 if (records) {
-#pragma unroll
-                    for (int c = 0; c < C; ++c) uptr[c] = u[c];
+                    static_assert(C == 2, "u records are written as pairs");
+                    ring_put2(rp.ring, rp.bf16, uidx, u[0], u[1]);
                 }
             }
             optr += p.out_ss;
-            if (records) uptr += rp.stride;
+            uidx += rp.stride;
             s.advance(tk + base, u, alpha);  // S <- k^ u^T + alpha S
             const int step = cb + tt;  // token index inside the row
             if constexpr (MODE == Mode::Snap) {

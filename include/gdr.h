@@ -142,12 +142,13 @@ int gdr_output_shape(int64_t total_tokens, int32_t nv, int32_t V, int64_t out_sh
 
 /* Minimum ring record length in elements for GQA ratio `ratio` = nv/nk
  * ("gated_delta_recurrence_verify_ring_gpu", ring_record_stride: at least
- * gated_delta_ring_record_elements(nv // nk)).  Record layout, float32:
- *     [ k^ (K) | alpha_0 .. alpha_{ratio-1}, padded to a multiple of 4 |
+ * gated_delta_ring_record_elements(nv // nk)).  Record layout, in elements of
+ * the ring's dtype:
+ *     [ k^ (K) | alpha_0 .. alpha_{ratio-1}, padded to a multiple of 8 |
  *       u_0 (V) | ... | u_{ratio-1} (V) ]
- * (the padding floats are never written or read)
- * where u_j and alpha_j belong to value head hk*ratio + j.  Returns the length
- * (K + 4*ceil(ratio/4) + ratio*V) or a negative code. */
+ * (the padding elements are never written or read) where u_j and alpha_j
+ * belong to value head hk*ratio + j.  Returns the length
+ * (K + 8*ceil(ratio/8) + ratio*V) or a negative code. */
 int gdr_ring_record_elements(int32_t K, int32_t V, int32_t ratio);
 
 /* Forward pass ("gated_delta_recurrence_fwd_gpu"): runs every row over its
@@ -162,10 +163,13 @@ int gdr_fwd(const gdr_step_args *args, void *stream);
  * A row with L <= ring_len writes record t - offsets[b] of
  *     ring[ring_slot_idx[b], hk, :, :]   (ring is [ring_rows, nk, ring_len, record_stride])
  * for each token, in the layout of gdr_ring_record_elements.  Padding rows
- * write no records.  ring_dtype must be GDR_F32 (the fold is bit-exact against
- * the forward pass only for float32 records); record_stride must be a multiple
- * of 4 and at least gdr_ring_record_elements(K, V, nv/nk); 1 <= ring_len <= 32. */
-int gdr_verify_ring(const gdr_step_args *args, float *ring, int32_t ring_dtype,
+ * write no records.  ring_dtype is GDR_F32 or GDR_BF16 (Parameters: ring_dtype;
+ * bfloat16 records are rounded to nearest-even once, and only a float32 ring
+ * keeps the fold bit-exact against the forward pass); the ring must be
+ * 16-byte aligned; record_stride must be a multiple of 4 (float32) or 8
+ * (bfloat16) and at least gdr_ring_record_elements(K, V, nv/nk);
+ * 1 <= ring_len <= 32. */
+int gdr_verify_ring(const gdr_step_args *args, void *ring, int32_t ring_dtype,
                     int64_t ring_rows, int32_t ring_len, int64_t record_stride,
                     const int32_t *ring_slot_idx, void *stream);
 
@@ -175,9 +179,11 @@ int gdr_verify_ring(const gdr_step_args *args, float *ring, int32_t ring_dtype,
  * writes it back.  counts[b] == 0 or counts[b] > ring_len leaves the row alone
  * (a row longer than ring_len was already committed by the verify pass, so a
  * caller passes its full length).  With a float32 ring the result equals
- * gdr_fwd over the accepted prefix bit for bit.  Uses from `args`: batch, nv,
+ * gdr_fwd over the accepted prefix bit for bit; a bfloat16 ring is widened
+ * exactly.  The ring needs element alignment only (16 bytes for the fast
+ * kernel).  Uses from `args`: batch, nv,
  * nk, K, V, state*, max_slots, slot_idx (qkv/decay/beta/out/offsets unused). */
-int gdr_fold(const gdr_step_args *args, const float *ring, int32_t ring_dtype,
+int gdr_fold(const gdr_step_args *args, const void *ring, int32_t ring_dtype,
              int64_t ring_rows, int32_t ring_len, int64_t record_stride,
              const int32_t *ring_slot_idx, const int32_t *counts, void *stream);
 

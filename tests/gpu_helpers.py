@@ -86,7 +86,20 @@ def check_state(gpu_state: np.ndarray, ref_state: np.ndarray, slots=None):
             assert rel <= F32_STATE_TOL, f"max rel state error {rel:.3e}"
 
 
-def ring_for(w: W.Workload, ring_len: int, rows: int) -> torch.Tensor:
+def ring_for(w: W.Workload, ring_len: int, rows: int, dtype=torch.float32) -> torch.Tensor:
     stride = gdr.gdr_ring_record_elements(w.K, w.V, w.nv // w.nk)
-    stride = (stride + 3) // 4 * 4
-    return torch.full((rows, w.nk, ring_len, stride), float("nan"), dtype=torch.float32, device=DEV)
+    stride = (stride + 7) // 8 * 8
+    return torch.full((rows, w.nk, ring_len, stride), float("nan"), dtype=dtype, device=DEV)
+
+
+def ring_to_host(t: torch.Tensor) -> np.ndarray:
+    """float32 ring as float32, bfloat16 ring as its uint16 bits."""
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def ring_to_dev(a: np.ndarray) -> torch.Tensor:
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16).copy()).to(DEV).view(torch.bfloat16)
+    return torch.from_numpy(a.copy()).to(DEV)

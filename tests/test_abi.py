@@ -65,8 +65,8 @@ def test_helpers(lib):
     assert lib.gdr_output_shape(647, 32, 128, shp) == 0
     assert (shp[0], shp[1]) == (647, 4096)
     assert lib.gdr_output_shape(-1, 32, 128, shp) == B.GDR_ERR_INVALID_ARG
-    assert lib.gdr_ring_record_elements(128, 128, 2) == 388
-    assert lib.gdr_ring_record_elements(16, 16, 1) == 36
+    assert lib.gdr_ring_record_elements(128, 128, 2) == 392
+    assert lib.gdr_ring_record_elements(16, 16, 1) == 40
     assert lib.gdr_ring_record_elements(64, 64, 5) == 64 + 8 + 320
     assert lib.gdr_ring_record_elements(0, 16, 1) == B.GDR_ERR_INVALID_ARG
 
@@ -128,8 +128,23 @@ def test_verify_and_fold_reject_bad_ring(lib):
     fake = 0x7f0000000000
     need = lib.gdr_ring_record_elements(16, 16, 2)
     a.state_dtype = B.GDR_F32
-    # bad ring dtype, length, stride, null pointers
-    assert lib.gdr_verify_ring(ctypes.byref(a), fake, B.GDR_BF16, 4, 8, need, fake, None) == \
+    # bad ring dtype, length, stride, alignment, null pointers
+    assert lib.gdr_verify_ring(ctypes.byref(a), fake, 7, 4, 8, need, fake, None) == \
+        B.GDR_ERR_UNSUPPORTED
+    assert need % 8 == 0
+    assert lib.gdr_verify_ring(ctypes.byref(a), fake, B.GDR_BF16, 4, 8, need + 4, fake, None) == \
+        B.GDR_ERR_INVALID_ARG  # a bfloat16 record stride must keep 16-byte records
+    assert lib.gdr_verify_ring(ctypes.byref(a), fake + 4, B.GDR_F32, 4, 8, need, fake, None) == \
+        B.GDR_ERR_UNSUPPORTED  # the verify pass writes 16-byte vectors
+    assert lib.gdr_verify_ring(ctypes.byref(a), fake + 8, B.GDR_BF16, 4, 8, need, fake, None) == \
+        B.GDR_ERR_UNSUPPORTED
+    # the fold reads elements: an element-aligned ring passes the ring checks and
+    # stops at the missing counts
+    assert lib.gdr_fold(ctypes.byref(a), fake + 4, B.GDR_F32, 4, 8, need, fake, None, None) == \
+        B.GDR_ERR_INVALID_ARG
+    assert lib.gdr_fold(ctypes.byref(a), fake + 2, B.GDR_BF16, 4, 8, need, fake, None, None) == \
+        B.GDR_ERR_INVALID_ARG
+    assert lib.gdr_fold(ctypes.byref(a), fake + 2, B.GDR_F32, 4, 8, need, fake, None, None) == \
         B.GDR_ERR_UNSUPPORTED
     assert lib.gdr_verify_ring(ctypes.byref(a), fake, B.GDR_F32, 4, 0, need, fake, None) == \
         B.GDR_ERR_UNSUPPORTED

@@ -59,6 +59,29 @@ def test_verify_output_equals_forward_and_pool_untouched(state_dtype):
             assert (host[s] == pool[s]).all(), "verify must leave the pool alone"
 
 
+@pytest.mark.parametrize("hint", [0, 12])  # general kernel / short-row kernel
+def test_bf16_ring_verify_matches_f32_ring_verify(hint):
+    """The ring dtype changes only the records: same output, same pool, and the
+    bfloat16 records are the float32 records rounded to nearest-even."""
+    w = W.verify_fold(batch=24, max_slots=48, ring_rows=48, nk=4, nv=8)
+    pool = w.state_pool()
+    rsi = torch.from_numpy(w.ring_slot_idx).to(DEV)
+    res = []
+    for dt in (torch.float32, torch.bfloat16):
+        d = Dev(w, pool)
+        ring = ring_for(w, w.ring_len, w.ring_rows, dt)
+        out = d.verify(ring, rsi, max_row_len=hint)
+        torch.cuda.synchronize()
+        res.append((out.cpu().numpy(), pool_to_host(d.state), ring))
+    assert (res[0][0].view(np.uint32) == res[1][0].view(np.uint32)).all()
+    assert (res[0][1] == res[1][1]).all()
+    r32, r16 = res[0][2], res[1][2]
+    written = ~torch.isnan(r32)
+    assert (written == ~torch.isnan(r16)).all()
+    # compare written fields only (torch's NaN conversion picks its own bits)
+    assert (r32.to(torch.bfloat16).view(torch.int16)[written] == r16.view(torch.int16)[written]).all()
+
+
 @pytest.mark.parametrize("K", [32, 64, 128])
 @pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
 def test_verify_plus_fold_equals_forward_over_prefix(state_dtype, K):
@@ -335,16 +358,17 @@ def test_short_row_kernel_equals_general_kernel(state_dtype):
     assert st == 0, gdr.status_names(st)  # the 20-token row has exactly n_inter = 6 drafts of 3
 
 
+@pytest.mark.parametrize("ring_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("K", [16, 32, 64, 128])
 @pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
-def test_sliced_fold_equals_simple_fold(state_dtype, K):
+def test_sliced_fold_equals_simple_fold(state_dtype, K, ring_dtype):
     """A 16-byte-aligned ring takes the row-slice fold (where the head size
-    allows it), a view offset by one float takes the simple one: same bits."""
+    allows it), a view offset by one element takes the simple one: same bits."""
     kw = {} if K == 128 else dict(nk=2, nv=6, K=K)
     w = W.verify_fold(batch=40, max_slots=64, ring_rows=64, state_dtype=state_dtype, **kw)
     pool = w.state_pool()
     d = Dev(w, pool)
-    ring = ring_for(w, w.ring_len, w.ring_rows)
+    ring = ring_for(w, w.ring_len, w.ring_rows, ring_dtype)
     rsi = torch.from_numpy(w.ring_slot_idx).to(DEV)
     d.verify(ring, rsi, max_row_len=12)
     cnt = torch.from_numpy(w.counts).to(DEV)
@@ -352,7 +376,7 @@ def test_sliced_fold_equals_simple_fold(state_dtype, K):
     for shifted in (False, True):
         st = pool_to_dev(pool_to_host(d.state))
         if shifted:
-            buf = torch.empty(ring.numel() + 1, device=DEV)
+            buf = torch.empty(ring.numel() + 1, dtype=ring_dtype, device=DEV)
             buf[1:] = ring.reshape(-1)
             r = buf[1:].view(ring.shape)
         else:

@@ -14,8 +14,8 @@ import torch
 import oracle
 import gated_deltanet_linear_gdr_gb300 as gdr
 from gated_deltanet_linear_gdr_gb300 import workloads as W
-from tests.gpu_helpers import (DEV, Dev, check_out, check_state, pool_to_dev, pool_to_host,
-                               ring_for)
+from tests.gpu_helpers import (DEV, Dev, as_f64, check_out, check_state, pool_to_dev, pool_to_host,
+                               ring_for, ring_to_dev, ring_to_host)
 from tests.helpers import problem, sub_workload
 
 pytestmark = pytest.mark.gpu
@@ -177,6 +177,41 @@ def test_fold_on_synthetic_ring(state_dtype):
     for b, s in enumerate(w.slot_idx):
         if s >= 0 and (counts[b] == 0 or counts[b] > ring_len):
             assert (host[s] == pool[s]).all()
+
+
+@pytest.mark.parametrize("hint", [0, 12])  # 0: general kernel; 12: short-row kernel
+@pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
+def test_bf16_ring_verify_records_and_fold(state_dtype, hint):
+    """bfloat16 ring ("gated_delta_recurrence_verify_ring_gpu" Parameters:
+    ring_dtype): verify writes the forward pass's output and records within one
+    bfloat16 ulp of the oracle's (each side rounds its own value once); the fold
+    of the oracle's bfloat16 records matches the oracle's fold of them."""
+    w = W.verify_fold(batch=24, max_slots=48, ring_rows=48, nk=4, nv=8, state_dtype=state_dtype)
+    pool = w.state_pool()
+    d = Dev(w, pool)
+    ring = ring_for(w, w.ring_len, w.ring_rows, torch.bfloat16)
+    rsi = torch.from_numpy(w.ring_slot_idx).to(DEV)
+    out = d.verify(ring, rsi, max_row_len=hint)
+    torch.cuda.synchronize()
+    pv = problem(w, state=pool.copy())
+    oring = np.full(tuple(ring.shape), 0x7FC0, np.uint16)
+    ref = oracle.verify_ring(pv, oring, w.ring_slot_idx, w.ring_len)
+    check_out(out, ref)
+    g = ring_to_host(ring)
+    nan = 0x7FC0
+    assert ((g == nan) == (oring == nan)).all(), "same record fields written"
+    m = oring != nan
+    gf, rf = as_f64(g[m]), as_f64(oring[m])
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(rf), 2.0 ** -20))) - 7)
+    bad = np.abs(gf - rf) > ulp * 1.001
+    assert not bad.any(), f"{int(bad.sum())} of {bad.size} records beyond one bfloat16 ulp"
+    # fold the oracle's records on the GPU and in the oracle
+    st = pool_to_dev(pool)
+    gdr.gdr_fold(st, d.slot, ring_to_dev(oring), rsi, torch.from_numpy(w.counts).to(DEV))
+    torch.cuda.synchronize()
+    pf = problem(w, state=pool.copy())
+    oracle.fold(pf, oring, w.ring_slot_idx, w.counts, w.ring_len)
+    check_state(pool_to_host(st), pf.state, slots=w.live_slots())
 
 
 @pytest.mark.parametrize("hint", [0, 8])  # 0: general kernel; 8: short-row kernel

@@ -7,7 +7,8 @@ consume what it produces.  All arrays are host numpy arrays in the layouts of
 
   qkv      [T, 2*nk*K + nv*V] float32: Q | K | V channel ranges, heads contiguous
   decay    [T, nv] float32: multiplicative decay alpha, or log decay g
-  beta     [T, nv] float32
+  beta     [T, nv] float32, or [T, nv, V] per value element
+           ("core.ssm.ops.gdp.fused_recurrent", beta [B, T, HV] or [B, T, HV, V])
   state    [slots, nv, K, V]: float32, or uint16 holding bfloat16 bits
   slot_idx [batch] int32, -1 = padding request
   offsets  [batch+1] int32, row b spans [offsets[b], offsets[b+1])
@@ -178,11 +179,12 @@ def verify_fold(seed: int = 3, batch: int = 128, draft: int = 5, long_len: int =
 
 def gdp_snapshots(seed: int = 4, batch: int = 64, drafts: int = 4, householder: int = 2,
                   max_slots: int = 128, nk: int = 16, nv: int = 32, K: int = 128,
-                  state_dtype: str = "f32") -> Workload:
+                  state_dtype: str = "f32", beta_per_value: bool = False) -> Workload:
     """Gated Delta Product spec-decode: `drafts` draft tokens x `householder` copies folded
     into the sequence ("core.ssm.ops.gdp.fused_recurrent", module summary): each step has
     its own k, v, beta and q; the log decay g ~ U(-0.1, 0) sits on the first copy of a
-    draft token and g = 0 on the others.  steps_per_token = householder."""
+    draft token and g = 0 on the others.  steps_per_token = householder.  beta is
+    head-wise, or per value element when beta_per_value."""
     rng = np.random.default_rng(seed)
     V = K
     Lr = drafts * householder
@@ -192,7 +194,7 @@ def gdp_snapshots(seed: int = 4, batch: int = 64, drafts: int = 4, householder: 
     g = rng.uniform(-0.1, 0.0, (T, nv)).astype(np.float32)
     step_in_row = np.arange(T) % Lr
     g[(step_in_row % householder) != 0] = 0.0
-    beta = _sigmoid(rng.standard_normal((T, nv))).astype(np.float32)
+    beta = _sigmoid(rng.standard_normal((T, nv, V) if beta_per_value else (T, nv))).astype(np.float32)
     slot_idx = rng.permutation(max_slots)[:batch].astype(np.int32)
     accepted = rng.integers(0, drafts, size=batch).astype(np.int32)
     return Workload("gdp_snapshots", nk, nv, K, V, qkv, g, beta, slot_idx, offsets,
@@ -203,8 +205,10 @@ def gdp_snapshots(seed: int = 4, batch: int = 64, drafts: int = 4, householder: 
 
 def random_case(seed: int, lengths, nk: int, nv: int, K: int, max_slots: int,
                 state_dtype: str = "f32", n_pad: int = 0, decay_is_log: bool = False,
-                use_l2norm: bool = True, scale: float = 0.0, state_std: float = 0.1) -> Workload:
-    """A small general case for parity tests: given row lengths, random slots."""
+                use_l2norm: bool = True, scale: float = 0.0, state_std: float = 0.1,
+                beta_per_value: bool = False) -> Workload:
+    """A small general case for parity tests: given row lengths, random slots;
+    beta per value element when beta_per_value."""
     rng = np.random.default_rng(seed)
     V = K
     L = np.asarray(lengths, dtype=np.int64)
@@ -216,7 +220,7 @@ def random_case(seed: int, lengths, nk: int, nv: int, K: int, max_slots: int,
         decay = rng.uniform(-0.1, 0.0, (T, nv)).astype(np.float32)
     else:
         decay = rng.uniform(0.8, 1.0, (T, nv)).astype(np.float32)
-    beta = rng.uniform(0.0, 1.0, (T, nv)).astype(np.float32)
+    beta = rng.uniform(0.0, 1.0, (T, nv, V) if beta_per_value else (T, nv)).astype(np.float32)
     slot_idx = rng.permutation(max_slots)[:batch].astype(np.int32)
     if n_pad:
         slot_idx[rng.choice(batch, size=n_pad, replace=False)] = -1

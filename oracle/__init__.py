@@ -13,7 +13,7 @@ matrix form used to pin the C loops on tiny cases.
 Arrays are dense and follow the pages' layouts:
   qkv    [T, 2*nk*K + nv*V] float32   ("gated_delta_recurrence_fwd_gpu", Args)
   decay  [T, nv] float32 (alpha, or log decay g when decay_is_log)
-  beta   [T, nv] float32
+  beta   [T, nv] float32 (head-wise) or [T, nv, V] (per value element)
   state  [max_slots, nv, K, V] float32, or uint16 holding bfloat16 bits
   slot_idx [batch] int32 (-1 = padding), offsets [batch+1] int32
 """
@@ -59,6 +59,7 @@ class _Problem(ctypes.Structure):
         ("state", ctypes.c_void_p), ("state_bf16", ctypes.c_int32),
         ("max_slots", ctypes.c_int64),
         ("slot_idx", ctypes.c_void_p), ("offsets", ctypes.c_void_p),
+        ("beta_per_value", ctypes.c_int32),
     ]
 
 
@@ -114,7 +115,10 @@ class Problem:
         T = self.qkv.shape[0] if self.qkv.ndim == 2 else 0
         self.total_tokens = T
         assert self.qkv.shape == (T, 2 * nk * K + nv * V), self.qkv.shape
-        assert self.decay.shape == (T, nv) and self.beta.shape == (T, nv)
+        assert self.decay.shape == (T, nv)
+        # beta: head-wise [T, nv] or per value element [T, nv, V]
+        assert self.beta.shape in ((T, nv), (T, nv, V)), self.beta.shape
+        self.beta_per_value = self.beta.ndim == 3
         assert state.ndim == 4 and state.shape[1:] == (nv, K, V), state.shape
         assert self.offsets.shape == (self.slot_idx.shape[0] + 1,)
 
@@ -126,7 +130,7 @@ class Problem:
             use_l2norm=int(self.use_l2norm), scale=self.scale, eps=self.eps,
             state=_ptr(self.state), state_bf16=int(self.state.dtype == np.uint16),
             max_slots=self.state.shape[0], slot_idx=_ptr(self.slot_idx),
-            offsets=_ptr(self.offsets))
+            offsets=_ptr(self.offsets), beta_per_value=int(self.beta_per_value))
 
     def _out(self):
         return np.zeros((self.total_tokens, self.nv * self.V), dtype=np.float64)

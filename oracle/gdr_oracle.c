@@ -21,7 +21,8 @@
  *     whose count exceeds RING_LEN.  Args: ring [ring_rows, nk, RING_LEN,
  *     ring_record_stride] indexed by ring_slot_idx[b].
  *   - "core.ssm.ops.gdp.fused_recurrent" (Megatron-Core), module summary and
- *     Parameters: g is a log decay (alpha = exp(g)); state_indices -1 marks a
+ *     Parameters: g is a log decay (alpha = exp(g)); beta is head-wise
+ *     [T, HV] or per value element [T, HV, V]; state_indices -1 marks a
  *     padding request (zero output, state untouched, no snapshot writes);
  *     intermediate_states[slot, i] holds the state after draft token i, i.e.
  *     after every steps_per_token recurrence steps.
@@ -68,7 +69,7 @@ typedef struct {
     int64_t total_tokens;
     const float *qkv;    /* [T, 2*nk*K + nv*V], dense                      */
     const float *decay;  /* [T, nv]: alpha, or g when decay_is_log          */
-    const float *beta;   /* [T, nv]                                         */
+    const float *beta;   /* [T, nv], or [T, nv, V] when beta_per_value      */
     int32_t decay_is_log, use_l2norm;
     double scale;        /* <= 0 selects K^-0.5                             */
     double eps;
@@ -77,6 +78,7 @@ typedef struct {
     int64_t max_slots;
     const int32_t *slot_idx; /* [batch], -1 = padding                       */
     const int32_t *offsets;  /* [batch + 1]                                 */
+    int32_t beta_per_value;
 } oracle_problem;
 
 /* ---- storage conversions (shared by both precisions) ------------------- */

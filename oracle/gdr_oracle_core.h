@@ -33,8 +33,8 @@ static REAL SFX(load_elem)(const void *base, int bf16, size_t idx)
  * Outputs: o (V), and the normalised key kh (K) and correction u (V) that a
  * verify record keeps. */
 static void SFX(token)(int K, int V, REAL *S, const float *q, const float *k,
-                       const float *v, REAL alpha, REAL beta, int l2, REAL scale,
-                       REAL eps, REAL *qh, REAL *kh, REAL *u, REAL *o)
+                       const float *v, REAL alpha, const float *beta, int beta_stride, int l2,
+                       REAL scale, REAL eps, REAL *qh, REAL *kh, REAL *u, REAL *o)
 {
     REAL nq = 1, nk = 1;
     if (l2) {
@@ -54,12 +54,13 @@ static void SFX(token)(int K, int V, REAL *S, const float *q, const float *k,
     for (int i = 0; i < K; ++i)
         for (int j = 0; j < V; ++j)
             S[(size_t)i * V + j] = alpha * S[(size_t)i * V + j];
-    /* delta rule: u = beta * (v - S^T k^) against the decayed state */
+    /* delta rule: u = beta * (v - S^T k^) against the decayed state; beta is
+     * one value for the head (beta_stride 0) or one per value column */
     for (int j = 0; j < V; ++j) {
         REAL w = 0;
         for (int i = 0; i < K; ++i)
             w += S[(size_t)i * V + j] * kh[i];
-        u[j] = beta * ((REAL)v[j] - w);
+        u[j] = (REAL)beta[(size_t)j * beta_stride] * ((REAL)v[j] - w);
     }
     /* rank-one update S += k^ u^T */
     for (int i = 0; i < K; ++i)
@@ -141,9 +142,11 @@ static int SFX(run)(const oracle_problem *p, double *out, void *ring, int ring_b
                 const float *v = row + (size_t)2 * nk * K + (size_t)h * V;
                 const float g = p->decay[(size_t)t * nv + h];
                 const REAL alpha = p->decay_is_log ? EXP((REAL)g) : (REAL)g;
-                const REAL beta = (REAL)p->beta[(size_t)t * nv + h];
-                SFX(token)(K, V, S, q, k, v, alpha, beta, p->use_l2norm, scale, eps,
-                           qh, kh, u, o);
+                const float *beta = p->beta_per_value
+                                         ? p->beta + ((size_t)t * nv + h) * (size_t)V
+                                         : p->beta + (size_t)t * nv + h;
+                SFX(token)(K, V, S, q, k, v, alpha, beta, p->beta_per_value ? 1 : 0, p->use_l2norm,
+                           scale, eps, qh, kh, u, o);
                 for (int j = 0; j < V; ++j)
                     out[(size_t)t * value_dim + (size_t)h * V + j] = (double)o[j];
                 if (records) {

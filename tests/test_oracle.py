@@ -343,6 +343,50 @@ def test_invalid_arguments_rejected():
         oracle.fwd(problem(dataclasses.replace(w, qkv=qkv), state=pool.copy(), nk=3))
 
 
+# ------------------------------------------------- per-element beta ---
+
+def test_beta_per_value_columns_equal_headwise_runs():
+    """beta [T, HV, V] ("core.ssm.ops.gdp.fused_recurrent" Parameters): the
+    columns of S evolve independently (each sees only its own a_j, u_j), so
+    column j of a run with per-element beta equals, exactly, column j of a run
+    whose head-wise beta is that column's value."""
+    levels = np.array([0.0, 0.25, 0.5, 1.0], np.float32)
+    w = _small(40, [4, 3], nk=1, nv=2, K=16, state_dtype="f32")
+    T, nv, V = w.total_tokens, w.nv, w.V
+    rng = np.random.default_rng(41)
+    pick = rng.integers(0, len(levels), size=(nv, V))       # one level per (head, column)
+    beta_pv = np.broadcast_to(levels[pick], (T, nv, V)).astype(np.float32).copy()
+    pool = w.state_pool()
+    pp = problem(dataclasses.replace(w, beta=beta_pv), state=pool.copy())
+    out_pv = oracle.fwd(pp)
+    for li, lv in enumerate(levels):
+        ph = problem(dataclasses.replace(w, beta=np.full((T, nv), lv, np.float32)), state=pool.copy())
+        out_h = oracle.fwd(ph)
+        for h in range(nv):
+            cols = np.nonzero(pick[h] == li)[0]
+            if cols.size == 0:
+                continue
+            assert (out_pv[:, h * V + cols] == out_h[:, h * V + cols]).all()
+            for s in w.slot_idx:
+                assert (pp.state[s, h][:, cols] == ph.state[s, h][:, cols]).all()
+
+
+def test_beta_per_value_zero_column_only_decays():
+    """beta_j = 0 makes u_j = 0: column j of S is only decayed, token by token."""
+    w = _small(42, [3], nk=1, nv=1, K=16, state_dtype="f32")
+    T, V = w.total_tokens, w.V
+    beta = np.full((T, 1, V), 0.7, np.float32)
+    beta[:, 0, 5] = 0.0
+    pool = w.state_pool()
+    p = problem(dataclasses.replace(w, beta=beta), state=pool.copy())
+    oracle.fwd(p)
+    s = int(w.slot_idx[0])
+    decay = np.prod(w.decay[:, 0].astype(np.float64))
+    np.testing.assert_allclose(p.state[s, 0][:, 5], decay * pool[s, 0][:, 5].astype(np.float64),
+                               rtol=1e-6)
+    assert not np.allclose(p.state[s, 0][:, 4], decay * pool[s, 0][:, 4])
+
+
 # ---------------------------------------------------------- verify / fold ---
 
 def _ring(w, nk, ring_len, rows, bf16=False):

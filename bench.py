@@ -47,7 +47,8 @@ def parse():
     ap.add_argument("--impl", default="gdr", choices=["gdr", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "verify_fold", "verify_fold_bf16_ring", "gdp_snapshots"],
+    ap.add_argument("--only", choices=["prefill", "verify_fold", "verify_fold_bf16_ring", "gdp_snapshots",
+                                       "gdp_snapshots_beta_per_value"],
                     default=None,
                     help="time just this secondary workload and print its figures (profiling aid)")
     ap.add_argument("--soak-s", type=float, default=1.0,
@@ -337,12 +338,12 @@ def bench_verify_fold(dev, flush, stream, hbm_peak, steps, ring_dtype=None):
     }
 
 
-def bench_gdp_snapshots(dev, flush, stream, hbm_peak, steps):
+def bench_gdp_snapshots(dev, flush, stream, hbm_peak, steps, beta_per_value=False):
     """Gated Delta Product drafts with snapshots (fp32 cache), then rollback."""
     import torch
     import gated_deltanet_linear_gdr_gb300 as gdr
     from gated_deltanet_linear_gdr_gb300 import workloads as W
-    w = W.gdp_snapshots()
+    w = W.gdp_snapshots(beta_per_value=beta_per_value)
     st = _pool_dev(w, dev)
     qkv, dec, bet, slot, off = (_to_dev(x, dev) for x in (w.qkv, w.decay, w.beta, w.slot_idx, w.offsets))
     inter = torch.zeros((w.max_slots, w.n_inter, w.nv, w.K, w.V), device=dev)
@@ -357,12 +358,16 @@ def bench_gdp_snapshots(dev, flush, stream, hbm_peak, steps):
     ts = statistics.median(time_steps(s_fn, steps, flush, stream))
     tr = statistics.median(time_steps(r_fn, steps, flush, stream))
     sbytes = decode_bytes(w, 4) + w.batch * w.n_inter * w.nv * w.K * w.V * 4
+    if beta_per_value:  # beta [T, nv, V] instead of [T, nv]
+        sbytes += w.total_tokens * w.nv * (w.V - 1) * 4
     rbytes = w.batch * w.nv * w.K * w.V * 4 * 2
     ht = w.live_head_tokens
     return {
         "workload": "GDP spec-decode: 64 requests x 4 drafts x 2 Householder copies (T=8 each), "
                     "spt=2, nk=16, nv=32, K=V=128, fp32 cache [128,32,128,128], "
-                    "intermediate [128,4,32,128,128]; then rollback",
+                    "intermediate [128,4,32,128,128]"
+                    + (", beta per value element [T,32,128]" if beta_per_value else "")
+                    + "; then rollback",
         "snapshots_ms": ts, "rollback_ms": tr, "head_tokens_per_s": ht / (ts * 1e-3),
         "snapshots_hbm_gbs": sbytes / (ts * 1e-3) / 1e9, "rollback_hbm_gbs": rbytes / (tr * 1e-3) / 1e9,
         "frac_hbm_snapshots": sbytes / (ts * 1e-3) / 1e9 / hbm_peak,
@@ -376,9 +381,15 @@ def bench_verify_fold_bf16_ring(dev, flush, stream, hbm_peak, steps):
     return bench_verify_fold(dev, flush, stream, hbm_peak, steps, ring_dtype=torch.bfloat16)
 
 
+def bench_gdp_snapshots_beta_per_value(dev, flush, stream, hbm_peak, steps):
+    """The snapshot workload with beta per value element (general kernel)."""
+    return bench_gdp_snapshots(dev, flush, stream, hbm_peak, steps, beta_per_value=True)
+
+
 SECONDARY = {"prefill": bench_prefill, "verify_fold": bench_verify_fold,
              "verify_fold_bf16_ring": bench_verify_fold_bf16_ring,
-             "gdp_snapshots": bench_gdp_snapshots}
+             "gdp_snapshots": bench_gdp_snapshots,
+             "gdp_snapshots_beta_per_value": bench_gdp_snapshots_beta_per_value}
 
 
 def secondary(dev, flush, stream, hbm_peak, steps, only=None):

@@ -52,6 +52,8 @@ class gdr_step_args(ctypes.Structure):
         ("state_head_stride", ctypes.c_int64), ("state_kdim_stride", ctypes.c_int64),
         ("state_vdim_stride", ctypes.c_int64), ("max_slots", ctypes.c_int64),
         ("slot_idx", ctypes.c_void_p), ("offsets", ctypes.c_void_p),
+        ("beta_seq_stride", ctypes.c_int64), ("beta_head_stride", ctypes.c_int64),
+        ("beta_vdim_stride", ctypes.c_int64),
     ]
 
 
@@ -158,8 +160,15 @@ def make_args(qkv, decay, beta, state, slot_idx, offsets, out, *, nk: int,
         if qkv.shape[1] != 2 * nk * K + nv * V:
             raise ValueError(f"qkv has {qkv.shape[1]} channels, expected 2*nk*K + nv*V = "
                              f"{2 * nk * K + nv * V}")
-        if decay.shape != (T, nv) or beta.shape != (T, nv) or decay.stride() != beta.stride():
-            raise ValueError("decay and beta must both be [T, nv] with the same strides")
+        if decay.shape != (T, nv):
+            raise ValueError("decay must be [T, nv]")
+        if beta.shape == (T, nv, V):
+            # per value element ("core.ssm.ops.gdp.fused_recurrent", beta [B, T, HV, V])
+            a.beta_seq_stride, a.beta_head_stride, a.beta_vdim_stride = beta.stride()
+            if a.beta_vdim_stride <= 0:
+                raise ValueError("per-element beta needs a positive value-dim stride")
+        elif beta.shape != (T, nv) or decay.stride() != beta.stride():
+            raise ValueError("beta must be [T, nv] with decay's strides, or [T, nv, V]")
         if out.shape != (T, nv * V):
             raise ValueError(f"out must be [T, nv*V] = [{T}, {nv * V}]")
         if offsets.shape != (batch + 1,) or not offsets.is_contiguous():

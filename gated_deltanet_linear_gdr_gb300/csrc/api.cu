@@ -107,6 +107,10 @@ int check_step(const gdr_step_args *a, const char *fn) {
             return fail(GDR_ERR_INVALID_ARG, "%s: token/output strides must be positive", fn);
     }
     if (!(a->eps >= 0.0f)) return fail(GDR_ERR_INVALID_ARG, "%s: eps must be >= 0", fn);
+    if (a->beta_vdim_stride < 0)
+        return fail(GDR_ERR_INVALID_ARG, "%s: beta_vdim_stride < 0", fn);
+    if (a->beta_vdim_stride > 0 && a->total_tokens > 0 && (a->beta_seq_stride <= 0 || a->beta_head_stride <= 0))
+        return fail(GDR_ERR_INVALID_ARG, "%s: per-element beta strides must be positive", fn);
     return GDR_OK;
 }
 
@@ -126,6 +130,12 @@ gdr::StepParams lower(const gdr_step_args *a, unsigned *status) {
     p.beta = a->beta;
     p.tok_ss = a->tok_seq_stride;
     p.tok_hs = a->tok_head_stride;
+    p.bpv = a->beta_vdim_stride > 0 ? 1 : 0;
+    p.beta_ss = a->beta_seq_stride;
+    p.beta_hs = a->beta_head_stride;
+    p.beta_vs = a->beta_vdim_stride;
+    p.beta_vec = (p.bpv && a->beta_vdim_stride == 1 && aligned16(a->beta) && a->beta_seq_stride % 4 == 0 &&
+                  a->beta_head_stride % 4 == 0) ? 1 : 0;
     p.scale = a->scale > 0.0f ? a->scale : (float)(1.0 / std::sqrt((double)a->K));
     p.eps = a->eps;
     p.out = a->out;
@@ -151,7 +161,8 @@ constexpr long long kShortRowMax = 64;
 cudaError_t launch_rows(const gdr::StepParams &p, const gdr_step_args *a, gdr::Mode mode, const gdr::RingParams &rp,
                         const gdr::SnapParams &sp, cudaStream_t s) {
     const bool bf16 = a->state_dtype == GDR_BF16;
-    if (a->max_row_len >= 1 && a->max_row_len <= kShortRowMax) {
+    // per-element beta runs on the general kernel only
+    if (!p.bpv && a->max_row_len >= 1 && a->max_row_len <= kShortRowMax) {
         bool used = false;
         cudaError_t e = gdr::launch_short(p, a->K, bf16, mode, rp, sp, a->max_row_len, s, &used);
         if (used || e != cudaSuccess) return e;
@@ -229,7 +240,8 @@ int gdr_fwd(const gdr_step_args *a, void *stream) {
     if ((rc = status_ptr(&st))) return rc;
     const gdr::StepParams p = lower(a, st);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (a->max_row_len == 1) return launched(gdr::launch_decode(p, a->K, a->state_dtype == GDR_BF16, s), "gdr_fwd");
+    if (a->max_row_len == 1 && !p.bpv)
+        return launched(gdr::launch_decode(p, a->K, a->state_dtype == GDR_BF16, s), "gdr_fwd");
     return launched(launch_rows(p, a, gdr::Mode::Fwd, gdr::RingParams{}, gdr::SnapParams{}, s), "gdr_fwd");
 }
 
@@ -237,6 +249,8 @@ int gdr_verify_ring(const gdr_step_args *a, void *ring, int32_t ring_dtype, int6
                     int32_t ring_len, int64_t record_stride, const int32_t *ring_slot_idx, void *stream) {
     int rc = check_step(a, "gdr_verify_ring");
     if (rc) return rc;
+    if (a->beta_vdim_stride > 0)
+        return fail(GDR_ERR_UNSUPPORTED, "gdr_verify_ring: beta must be [total_tokens, nv] (beta_vdim_stride 0)");
     const int r = a->nv / a->nk;
     rc = check_ring(ring_dtype, ring_rows, ring_len, record_stride, ring, ring_slot_idx, a->K, a->V, r,
                     a->batch, true, "gdr_verify_ring");

@@ -26,6 +26,9 @@ struct StepParams {
     long long st_slot, st_head, st_k;  // value-dim stride is 1
     long long max_slots;
     const int *slot_idx, *offsets;
+    int bpv;      // beta per value element: element (t, h, j) at t*beta_ss + h*beta_hs + j*beta_vs
+    long long beta_ss, beta_hs, beta_vs;
+    int beta_vec; // per-element beta rows may be read with 16-byte vector loads
     int qkv_vec;  // Q/K/V rows may be read with 16-byte vector loads
     int out_vec;  // output rows may be written with 16-byte vector stores
     unsigned *status;

@@ -20,7 +20,9 @@
 
 namespace gdr {
 
-template <typename ST, int K> struct ChainShape {
+// BPV: beta per value element, staged per token like v (then 8 tokens per chunk
+// keep the CTA's static shared memory under 48 KiB).
+template <typename ST, int K, bool BPV = false> struct ChainShape {
     static constexpr int V = K;
     static constexpr int NG = K / 8;               // row groups
     static constexpr int LK = NG >= 4 ? cmin(4, NG / 2) : NG;  // lanes along K
@@ -35,7 +37,7 @@ template <typename ST, int K> struct ChainShape {
     static constexpr int VS = W * WC;              // columns per CTA
     static constexpr int SLICES = V / VS;
     static constexpr int KP = K + LK * 4;          // padded staged vector length
-    static constexpr int TC = 16;                  // tokens per staged chunk
+    static constexpr int TC = BPV ? 8 : 16;        // tokens per staged chunk
     static constexpr int NL = NG / (RPAIR ? 2 : 1);  // lanes per token when normalising
     static constexpr int TPW = 32 / NL;            // tokens per warp when normalising
     using State = LaneState<RG, C>;
@@ -44,10 +46,10 @@ template <typename ST, int K> struct ChainShape {
 // Shared-memory index of raw row i (natural order, padded every ROWS rows).
 template <int ROWS> __device__ __forceinline__ int pidx(int i) { return vpos<false, ROWS>(i); }
 
-template <typename ST, int K, Mode MODE>
-__global__ void __launch_bounds__(ChainShape<ST, K>::NT, 4)
+template <typename ST, int K, Mode MODE, bool BPV>
+__global__ void __launch_bounds__(ChainShape<ST, K, BPV>::NT, 4)
     k_chain(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len) {
-    using Sh = ChainShape<ST, K>;
+    using Sh = ChainShape<ST, K, BPV>;
     constexpr int V = K, LK = Sh::LK, ROWS = Sh::ROWS, C = Sh::C;
     constexpr int WC = Sh::WC, W = Sh::W, NT = Sh::NT, VS = Sh::VS, SLICES = Sh::SLICES;
     constexpr int KP = Sh::KP, TC = Sh::TC, NL = Sh::NL, TPW = Sh::TPW;
@@ -57,6 +59,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT, 4)
     __shared__ __align__(16) float k_s[2][TC][KP];
     __shared__ __align__(16) float v_s[2][TC][VS];
     __shared__ __align__(16) float sc_s[2][TC][4];  // decay -> alpha, beta, k^.q~
+    __shared__ __align__(16) float b_s[BPV ? 2 : 1][BPV ? TC : 1][BPV ? VS : 4];  // per-element beta
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kl = lane % LK, vl = lane / LK;
@@ -124,6 +127,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT, 4)
     const long long qoff = (long long)(hk * K) * p.qkv_cs;
     const long long koff = (long long)(p.nk * K + hk * K) * p.qkv_cs;
     const long long voff = (long long)(2 * p.nk * K + h * V + slice * VS) * p.qkv_cs;
+    const float *bbase = p.beta + (long long)h * p.beta_hs + (long long)(slice * VS) * p.beta_vs;  // BPV
     bool overflow = false;
 
     // Raw operands of tokens [cb, cb + tc) into buffer bi; one cp.async group.
@@ -143,7 +147,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT, 4)
             for (int tt = tid; tt < tc; tt += NT) {
                 const long long o = (long long)(t0 + cb + tt) * p.tok_ss + (long long)h * p.tok_hs;
                 cp_async4(&sc_s[bi][tt][0], p.decay + o);
-                cp_async4(&sc_s[bi][tt][1], p.beta + o);
+                if constexpr (!BPV) cp_async4(&sc_s[bi][tt][1], p.beta + o);
             }
         } else {
             for (int idx = tid; idx < tc * K; idx += NT) {
@@ -159,7 +163,21 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT, 4)
             for (int tt = tid; tt < tc; tt += NT) {
                 const long long o = (long long)(t0 + cb + tt) * p.tok_ss + (long long)h * p.tok_hs;
                 sc_s[bi][tt][0] = p.decay[o];
-                sc_s[bi][tt][1] = p.beta[o];
+                if constexpr (!BPV) sc_s[bi][tt][1] = p.beta[o];
+            }
+        }
+        if constexpr (BPV) {
+            if (p.beta_vec) {
+                constexpr int RVS = VS / 4;
+                for (int idx = tid; idx < tc * RVS; idx += NT) {
+                    const int tt = idx / RVS, r = idx - tt * RVS;
+                    cp_async16(&b_s[bi][tt][4 * r], bbase + (long long)(t0 + cb + tt) * p.beta_ss + 4 * r);
+                }
+            } else {
+                for (int idx = tid; idx < tc * VS; idx += NT) {
+                    const int tt = idx / VS, j = idx - tt * VS;
+                    b_s[bi][tt][j] = bbase[(long long)(t0 + cb + tt) * p.beta_ss + (long long)j * p.beta_vs];
+                }
             }
         }
         cp_async_commit();
@@ -210,7 +228,8 @@ __global__ void __launch_bounds__(ChainShape<ST, K>::NT, 4)
             for (int c = 0; c < C; ++c) {
                 const float A = tree_lanes<LK>(a[c]);
                 const float B = tree_lanes<LK>(bq[c]);
-                u[c] = gdr_u(beta, alpha, A, vb[tt][wcol + c]);
+                const float bj = BPV ? b_s[BPV ? bi : 0][tt][wcol + c] : beta;
+                u[c] = gdr_u(bj, alpha, A, vb[tt][wcol + c]);
                 o[c] = gdr_o(alpha, B, kq, u[c]);
             }
             const int step = cb + tt;  // token index inside the row
@@ -273,17 +292,26 @@ template <typename ST, int K>
 static cudaError_t launch_chain_t(const StepParams &p, Mode mode, const RingParams &rp,
                                   const SnapParams &sp, long long max_len, cudaStream_t st) {
     using Sh = ChainShape<ST, K>;
+    static_assert(ChainShape<ST, K, true>::SLICES == Sh::SLICES && ChainShape<ST, K, true>::NT == Sh::NT,
+                  "same grid with per-element beta");
     const long long blocks = (long long)p.batch * p.nv * Sh::SLICES;
     if (blocks <= 0) return cudaGetLastError();
     switch (mode) {
         case Mode::Fwd:
-            k_chain<ST, K, Mode::Fwd><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+            if (p.bpv)
+                k_chain<ST, K, Mode::Fwd, true><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+            else
+                k_chain<ST, K, Mode::Fwd, false><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             break;
-        case Mode::Verify:
-            k_chain<ST, K, Mode::Verify><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+        case Mode::Verify:  // head-wise beta only
+            if (p.bpv) return cudaErrorInvalidValue;
+            k_chain<ST, K, Mode::Verify, false><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             break;
         case Mode::Snap:
-            k_chain<ST, K, Mode::Snap><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+            if (p.bpv)
+                k_chain<ST, K, Mode::Snap, true><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+            else
+                k_chain<ST, K, Mode::Snap, false><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             break;
     }
     return cudaGetLastError();

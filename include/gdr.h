@@ -79,6 +79,11 @@ typedef enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
  *          decay_is_log != 0 ("core.ssm.ops.gdp.fused_recurrent", g).
  * beta     [total_tokens, nv] float32.  decay and beta share tok_seq_stride /
  *          tok_head_stride ("per_token_seqlen_stride", "per_token_head_stride").
+ *          With beta_vdim_stride > 0, beta is per value element instead,
+ *          [total_tokens, nv, V] ("core.ssm.ops.gdp.fused_recurrent", beta
+ *          [B, T, HV, V]): element (t, h, j) at t*beta_seq_stride +
+ *          h*beta_head_stride + j*beta_vdim_stride, and u_j = beta_j (v_j - ...).
+ *          Forward and snapshot passes only (the verify pass takes [T, nv]).
  * out      [total_tokens, nv*V] float32; element (t, j) at t*out_seq_stride +
  *          j*out_vdim_stride.  Written for every token of every row.
  * state    [max_slots, nv, K, V] pool of state_dtype, read and written in place at
@@ -128,6 +133,9 @@ typedef struct gdr_step_args {
     int64_t max_slots;
     const int32_t *slot_idx;
     const int32_t *offsets;
+    int64_t beta_seq_stride;  /* per-element beta only (beta_vdim_stride > 0) */
+    int64_t beta_head_stride;
+    int64_t beta_vdim_stride; /* 0: beta is [total_tokens, nv] */
 } gdr_step_args;
 
 /* Message for the last error returned on this thread ("" if none). */

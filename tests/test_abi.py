@@ -49,14 +49,22 @@ def test_library_exports_nothing_else(lib):
     assert syms == set(declared_functions()), syms ^ set(declared_functions())
 
 
-def test_struct_layout_matches_header():
-    # int32 x 8, int64 x 2, then pointers/int64s; 200 bytes on LP64
-    assert ctypes.sizeof(B.gdr_step_args) == 200
-    assert B.gdr_step_args.total_tokens.offset == 32
-    assert B.gdr_step_args.qkv.offset == 48
-    assert B.gdr_step_args.scale.offset == 104
-    assert B.gdr_step_args.state.offset == 136
-    assert B.gdr_step_args.offsets.offset == 192
+def test_struct_layout_matches_header(tmp_path):
+    """The ctypes mirror has the C compiler's size and field offsets for the
+    struct in include/gdr.h."""
+    fields = [f[0] for f in B.gdr_step_args._fields_]
+    prog = tmp_path / "layout.c"
+    prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gdr.h"\nint main(void) {\n'
+                    '  printf("size %zu\\n", sizeof(gdr_step_args));\n' +
+                    "".join(f'  printf("{f} %zu\\n", offsetof(gdr_step_args, {f}));\n' for f in fields) +
+                    "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                        check=True).stdout.splitlines())
+    assert int(got["size"]) == ctypes.sizeof(B.gdr_step_args)
+    for f in fields:
+        assert int(got[f]) == getattr(B.gdr_step_args, f).offset, f
 
 
 def test_helpers(lib):
@@ -160,6 +168,19 @@ def test_verify_and_fold_reject_bad_ring(lib):
         B.GDR_ERR_INVALID_ARG  # counts NULL
     assert lib.gdr_fold(ctypes.byref(a), fake, B.GDR_F32, 0, 8, need, fake, fake, None) == \
         B.GDR_ERR_INVALID_ARG  # ring_rows 0
+
+
+def test_verify_rejects_per_element_beta(lib):
+    a = _valid_args()
+    a.V = a.K = 16
+    a.state_dtype = B.GDR_F32
+    fake = 0x7f0000000000
+    need = lib.gdr_ring_record_elements(16, 16, 2)
+    a.beta_seq_stride, a.beta_head_stride, a.beta_vdim_stride = 64, 16, 1
+    assert lib.gdr_verify_ring(ctypes.byref(a), fake, B.GDR_F32, 4, 8, need, fake, None) == \
+        B.GDR_ERR_UNSUPPORTED
+    a.beta_vdim_stride = -1
+    assert lib.gdr_fwd(ctypes.byref(a), None) == B.GDR_ERR_INVALID_ARG
 
 
 def test_snapshots_and_rollback_reject_bad_buffers(lib):

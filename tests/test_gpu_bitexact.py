@@ -59,6 +59,19 @@ def test_verify_output_equals_forward_and_pool_untouched(state_dtype):
             assert (host[s] == pool[s]).all(), "verify must leave the pool alone"
 
 
+@pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
+def test_beta_per_value_constant_along_v_equals_headwise(state_dtype):
+    """Per-element beta that is constant along V gives the head-wise result bit
+    for bit (same operation on every column)."""
+    w = W.random_case(620, [17, 3, 1], nk=2, nv=4, K=128, max_slots=6, state_dtype=state_dtype)
+    pool = w.state_pool()
+    out_h, pool_h = _run_fwd(w, pool)
+    wp = dataclasses.replace(w, beta=np.repeat(w.beta[:, :, None], w.V, axis=2).copy())
+    out_p, pool_p = _run_fwd(wp, pool)
+    assert (out_h.view(np.uint32) == out_p.view(np.uint32)).all()
+    assert (pool_h == pool_p).all()
+
+
 @pytest.mark.parametrize("hint", [0, 12])  # general kernel / short-row kernel
 def test_bf16_ring_verify_matches_f32_ring_verify(hint):
     """The ring dtype changes only the records: same output, same pool, and the

@@ -179,6 +179,43 @@ def test_fold_on_synthetic_ring(state_dtype):
             assert (host[s] == pool[s]).all()
 
 
+@pytest.mark.parametrize("K", [16, 32, 64, 128])
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("hint", [0, 1, 40])
+def test_beta_per_value_forward(K, state_dtype, hint):
+    """beta [T, HV, V] ("core.ssm.ops.gdp.fused_recurrent" Parameters) against
+    the oracle; ragged rows over several staged chunks, a padding row, every
+    kernel hint (per-element beta always runs on the general kernel)."""
+    lengths = [1, 19, 0, 9] if hint != 1 else [1, 1, 0, 1]
+    w = W.random_case(600 + K, lengths, nk=2, nv=4, K=K, max_slots=9, state_dtype=state_dtype,
+                      n_pad=1, beta_per_value=True)
+    _fwd_parity(w, max_row_len=hint)
+
+
+def test_beta_per_value_strided_and_snapshots():
+    """A non-contiguous per-element beta (scalar staging) and the snapshot pass."""
+    w = W.random_case(610, [8, 6, 8], nk=2, nv=4, K=64, max_slots=6, state_dtype="f32",
+                      beta_per_value=True, decay_is_log=True)
+    pool = w.state_pool()
+    d = Dev(w, pool)
+    bt = torch.from_numpy(np.ascontiguousarray(w.beta.transpose(2, 0, 1))).to(DEV)  # [V, T, nv]
+    d.beta = bt.permute(1, 2, 0)  # [T, nv, V] view with value-dim stride T*nv
+    inter = torch.full((w.max_slots, 4, w.nv, w.K, w.V), float("nan"), device=DEV)
+    out = d.snapshots(inter, 2)
+    torch.cuda.synchronize()
+    p = problem(w, state=pool.copy())
+    oint = np.full((w.max_slots, 4, w.nv, w.K, w.V), np.nan, np.float32)
+    ref = oracle.fwd_snapshots(p, oint, 2)
+    check_out(out, ref)
+    hi = inter.cpu().numpy()
+    written = ~np.isnan(oint)
+    assert (written == ~np.isnan(hi)).all(), "snapshot entries written where the oracle writes"
+    hi[~written] = 0.0
+    oint[~written] = 0.0
+    check_state(hi, oint)
+    check_state(pool_to_host(d.state), p.state)
+
+
 @pytest.mark.parametrize("hint", [0, 12])  # 0: general kernel; 12: short-row kernel
 @pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
 def test_bf16_ring_verify_records_and_fold(state_dtype, hint):

@@ -154,15 +154,17 @@ gdr::StepParams lower(const gdr_step_args *a, unsigned *status) {
     return p;
 }
 
-// Rows of at most this many tokens (by the caller's max_row_len promise) run on
-// the pipelined short-row kernel; longer or unknown lengths on the general one.
+// Forward and verify rows of at most this many tokens (by the caller's
+// max_row_len promise) run on the pipelined short-row kernel; longer or
+// unknown lengths on the general one.  Snapshot passes always take the general
+// kernel, which stores each snapshot straight from registers (measured faster
+// than staging it through shared memory), as does per-element beta.
 constexpr long long kShortRowMax = 64;
 
 cudaError_t launch_rows(const gdr::StepParams &p, const gdr_step_args *a, gdr::Mode mode, const gdr::RingParams &rp,
                         const gdr::SnapParams &sp, cudaStream_t s) {
     const bool bf16 = a->state_dtype == GDR_BF16;
-    // per-element beta runs on the general kernel only
-    if (!p.bpv && a->max_row_len >= 1 && a->max_row_len <= kShortRowMax) {
+    if (!p.bpv && mode != gdr::Mode::Snap && a->max_row_len >= 1 && a->max_row_len <= kShortRowMax) {
         bool used = false;
         cudaError_t e = gdr::launch_short(p, a->K, bf16, mode, rp, sp, a->max_row_len, s, &used);
         if (used || e != cudaSuccess) return e;

@@ -20,9 +20,11 @@
 
 namespace gdr {
 
-// BPV: beta per value element, staged per token like v (then 8 tokens per chunk
-// keep the CTA's static shared memory under 48 KiB).
-template <typename ST, int K, bool BPV = false> struct ChainShape {
+// Tokens per staged chunk: TCX = 16 in general, 8 for rows known to be that
+// short (a smaller stage, so more L1 is left) and for per-element beta (BPV:
+// beta staged per token like v; 8 tokens keep the static shared memory under
+// 48 KiB).
+template <typename ST, int K, bool BPV = false, int TCX = 16> struct ChainShape {
     static constexpr int V = K;
     static constexpr int NG = K / 8;               // row groups
     static constexpr int LK = NG >= 4 ? cmin(4, NG / 2) : NG;  // lanes along K
@@ -37,7 +39,7 @@ template <typename ST, int K, bool BPV = false> struct ChainShape {
     static constexpr int VS = W * WC;              // columns per CTA
     static constexpr int SLICES = V / VS;
     static constexpr int KP = K + LK * 4;          // padded staged vector length
-    static constexpr int TC = BPV ? 8 : 16;        // tokens per staged chunk
+    static constexpr int TC = BPV ? cmin(8, TCX) : TCX;  // tokens per staged chunk
     static constexpr int NL = NG / (RPAIR ? 2 : 1);  // lanes per token when normalising
     static constexpr int TPW = 32 / NL;            // tokens per warp when normalising
     using State = LaneState<RG, C>;
@@ -46,10 +48,10 @@ template <typename ST, int K, bool BPV = false> struct ChainShape {
 // Shared-memory index of raw row i (natural order, padded every ROWS rows).
 template <int ROWS> __device__ __forceinline__ int pidx(int i) { return vpos<false, ROWS>(i); }
 
-template <typename ST, int K, Mode MODE, bool BPV>
-__global__ void __launch_bounds__(ChainShape<ST, K, BPV>::NT, 4)
+template <typename ST, int K, Mode MODE, bool BPV, int TCX>
+__global__ void __launch_bounds__(ChainShape<ST, K, BPV, TCX>::NT, 4)
     k_chain(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len) {
-    using Sh = ChainShape<ST, K, BPV>;
+    using Sh = ChainShape<ST, K, BPV, TCX>;
     constexpr int V = K, LK = Sh::LK, ROWS = Sh::ROWS, C = Sh::C;
     constexpr int WC = Sh::WC, W = Sh::W, NT = Sh::NT, VS = Sh::VS, SLICES = Sh::SLICES;
     constexpr int KP = Sh::KP, TC = Sh::TC, NL = Sh::NL, TPW = Sh::TPW;
@@ -296,22 +298,25 @@ static cudaError_t launch_chain_t(const StepParams &p, Mode mode, const RingPara
                   "same grid with per-element beta");
     const long long blocks = (long long)p.batch * p.nv * Sh::SLICES;
     if (blocks <= 0) return cudaGetLastError();
+    const bool short_rows = max_len >= 1 && max_len <= 8;
     switch (mode) {
         case Mode::Fwd:
             if (p.bpv)
-                k_chain<ST, K, Mode::Fwd, true><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+                k_chain<ST, K, Mode::Fwd, true, 8><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             else
-                k_chain<ST, K, Mode::Fwd, false><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+                k_chain<ST, K, Mode::Fwd, false, 16><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             break;
         case Mode::Verify:  // head-wise beta only
             if (p.bpv) return cudaErrorInvalidValue;
-            k_chain<ST, K, Mode::Verify, false><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+            k_chain<ST, K, Mode::Verify, false, 16><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             break;
         case Mode::Snap:
             if (p.bpv)
-                k_chain<ST, K, Mode::Snap, true><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+                k_chain<ST, K, Mode::Snap, true, 8><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+            else if (short_rows)
+                k_chain<ST, K, Mode::Snap, false, 8><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             else
-                k_chain<ST, K, Mode::Snap, false><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+                k_chain<ST, K, Mode::Snap, false, 16><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             break;
     }
     return cudaGetLastError();

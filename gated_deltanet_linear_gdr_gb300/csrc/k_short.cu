@@ -1,7 +1,7 @@
-// Short-row pipelined kernel: forward, verify-ring and snapshot passes over
-// rows of a few tokens -- speculative-decoding verify windows
-// ("gated_delta_recurrence_verify_ring_gpu") and Gated Delta Product draft
-// sequences ("core.ssm.ops.gdp.fused_recurrent", intermediate_states).
+// Short-row pipelined kernel: forward and verify-ring passes over rows of a
+// few tokens -- speculative-decoding verify windows
+// ("gated_delta_recurrence_verify_ring_gpu").  (Snapshot passes run on the
+// general kernel, which stores snapshots straight from registers.)
 //
 // Persistent CTAs walk (row, value head, CW-column tile) units like the
 // pipelined decode kernel.  A unit's stage holds the bf16/f32 state tile and
@@ -14,8 +14,8 @@
 // butterfly over the LK lanes.  For each staged chunk the CTA's warps first
 // normalise the tokens (q~, k^ pair-interleaved, alpha and k^.q~ written back
 // into the stage; ring records get k^ and alpha here), then every warp runs
-// the chunk's tokens on its columns with warp shuffles only.  Snapshots and the final commit go
-// back through the stage and leave the SM as coalesced rows.  Rows longer than
+// the chunk's tokens on its columns with warp shuffles only.  The final commit
+// goes back through the stage and leaves the SM as coalesced rows.  Rows longer than
 // TCH load further chunks in place.  The arithmetic is the fixed sequence of
 // gdr_device.cuh, so results equal the other kernels' bit for bit.
 #include "gdr_pipe.cuh"
@@ -253,7 +253,6 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
     typename W::State s;
     short_get_tile<ST, K>(stage, r0, col, s);
     float *tokf = reinterpret_cast<float *>(stage + P::S_STATE);
-    bool overflow = false;
     // lanes kl == 0 write the output (and u records) of their C columns
     const bool w_out = kl == 0;
     long long uidx = ring_row + rp.u_off + jr * V + us * P::CW + col;  // this lane's u record
@@ -315,27 +314,7 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
             optr += p.out_ss;
             uidx += rp.stride;
             s.advance(tk + base, u, alpha);  // S <- k^ u^T + alpha S
-            const int step = cb + tt;  // token index inside the row
-            if constexpr (MODE == Mode::Snap) {
-                if ((step + 1) % sp.spt == 0) {
-                    const int i = (step + 1) / sp.spt - 1;
-                    if (i < sp.n_inter) {
-                        short_put_tile<ST, K>(stage, r0, col, s);
-                        __syncthreads();
-                        tile_store<ST, K, W::NT, kShortTileWarps, kShortSwizzle>(reinterpret_cast<ST *>(sp.inter) + (long long)m.slot * sp.s_slot +
-                                                     (long long)i * sp.s_tok + (long long)h * sp.s_head +
-                                                     us * P::CW,
-                                                 V, stage);
-                        __syncthreads();
-                    } else {
-                        overflow = true;
-                    }
-                }
-            }
         }
-    }
-    if constexpr (MODE == Mode::Snap) {
-        if (overflow && leader) flag(p.status, GDR_STATUS_SNAPSHOT_OVERFLOW);
     }
     if (commit) short_put_tile<ST, K>(stage, r0, col, s);
     return commit;
@@ -431,7 +410,7 @@ static cudaError_t launch_short_t(const StepParams &p, Mode mode, const RingPara
         switch (mode) {
             case Mode::Fwd: return launch_short_m<ST, K, Mode::Fwd>(p, rp, sp, max_len, st);
             case Mode::Verify: return launch_short_m<ST, K, Mode::Verify>(p, rp, sp, max_len, st);
-            case Mode::Snap: return launch_short_m<ST, K, Mode::Snap>(p, rp, sp, max_len, st);
+            case Mode::Snap: *used = false; return cudaSuccess;  // the general kernel takes snapshots
         }
     }
     return cudaSuccess;

@@ -150,6 +150,25 @@ def fwd(p: Problem, work: str = "f64") -> np.ndarray:
     return out
 
 
+def fwd_dense(qkv, decay, beta, offsets, initial_state, *, nk, nv, K, V, state_dtype="f32",
+              decay_is_log=False, use_l2norm=True, scale=0.0, eps=1e-6, work: str = "f64"):
+    """Forward pass with a dense start state ("core.ssm.ops.gdp.fused_recurrent",
+    initial_state [N, HV, K, V] or None for zeros, output_final_state): sequence n
+    starts from initial_state[n] and its final state is returned in a new
+    [N, HV, K, V] array (an empty sequence returns its initial state).  The
+    gather/scatter around the recurrence, written out: sequence n runs on slot n
+    of a pool that holds a copy of the start states.  Returns (out, final)."""
+    N = len(offsets) - 1
+    dt = np.uint16 if state_dtype == "bf16" else np.float32
+    pool = (np.zeros((N, nv, K, V), dt) if initial_state is None
+            else np.ascontiguousarray(initial_state, dtype=dt).copy())
+    assert pool.shape == (N, nv, K, V)
+    p = Problem(qkv, decay, beta, pool, np.arange(N, dtype=np.int32), offsets, nk=nk, nv=nv,
+                K=K, V=V, decay_is_log=decay_is_log, use_l2norm=use_l2norm, scale=scale, eps=eps)
+    out = fwd(p, work)
+    return out, pool
+
+
 def verify_ring(p: Problem, ring: np.ndarray, ring_slot_idx, ring_len: int,
                 work: str = "f64") -> np.ndarray:
     """Verify pass; writes records into ``ring`` [ring_rows, nk, ring_len, stride],

@@ -387,6 +387,46 @@ def test_beta_per_value_zero_column_only_decays():
     assert not np.allclose(p.state[s, 0][:, 4], decay * pool[s, 0][:, 4])
 
 
+# --------------------------------------------- dense initial / final state ---
+
+def _dense_inputs(w):
+    return dict(nk=w.nk, nv=w.nv, K=w.K, V=w.V, state_dtype=w.state_dtype, decay_is_log=w.decay_is_log,
+                use_l2norm=w.use_l2norm, scale=w.scale, eps=w.eps)
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_dense_state_equals_pool_at_the_rows_slots(state_dtype):
+    """initial_state / output_final_state ("core.ssm.ops.gdp.fused_recurrent"
+    Parameters) is the slot-indexed pass with the rows' states gathered densely:
+    same output, final[n] = the pool slot of row n after the pass, and an empty
+    row returns its initial state."""
+    w = _small(50, [4, 0, 7], nk=1, nv=2, K=16, state_dtype=state_dtype)
+    pool = w.state_pool()
+    pp = problem(w, state=pool.copy())
+    out_pool = oracle.fwd(pp)
+    init = pool[w.slot_idx].copy()
+    out_d, final = oracle.fwd_dense(w.qkv, w.decay, w.beta, w.offsets, init, **_dense_inputs(w))
+    assert (out_d == out_pool).all()
+    assert (final == pp.state[w.slot_idx]).all()
+    assert (final[1] == init[1]).all()
+
+
+def test_dense_state_without_initial_state_starts_from_zero():
+    """initial_state None means zeros: one token from S_0 = 0 gives
+    o = scale * beta * (k^ . q^) * v (readout of the updated state) and the
+    final state beta k^ v^T."""
+    w = _small(51, [1], nk=1, nv=1, K=16, state_dtype="f32")
+    out, final = oracle.fwd_dense(w.qkv, w.decay, w.beta, w.offsets, None, **_dense_inputs(w))
+    K = w.K
+    q = w.qkv[0, :K].astype(np.float64)
+    k = w.qkv[0, K:2 * K].astype(np.float64)
+    v = w.qkv[0, 2 * K:].astype(np.float64)
+    qh, kh = q / np.sqrt(q @ q + w.eps), k / np.sqrt(k @ k + w.eps)
+    b = float(w.beta[0, 0])
+    np.testing.assert_allclose(out[0], K ** -0.5 * b * (kh @ qh) * v, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(final[0, 0], (b * np.outer(kh, v)).astype(np.float32), rtol=1e-6)
+
+
 # ---------------------------------------------------------- verify / fold ---
 
 def _ring(w, nk, ring_len, rows, bf16=False):

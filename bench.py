@@ -47,7 +47,8 @@ def parse():
     ap.add_argument("--impl", default="gdr", choices=["gdr", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "verify_fold", "verify_fold_bf16_ring", "gdp_snapshots",
+    ap.add_argument("--only", choices=["prefill", "prefill_dense", "verify_fold", "verify_fold_bf16_ring",
+                                       "gdp_snapshots",
                                        "gdp_snapshots_beta_per_value"],
                     default=None,
                     help="time just this secondary workload and print its figures (profiling aid)")
@@ -285,6 +286,38 @@ def bench_prefill(dev, flush, stream, hbm_peak, steps):
     }
 
 
+def bench_prefill_dense(dev, flush, stream, hbm_peak, steps):
+    """The ragged prefill workload with a dense start and end state
+    (initial_state given, final state written to a second tensor)."""
+    import numpy as np
+    import torch
+    import gated_deltanet_linear_gdr_gb300 as gdr
+    from gated_deltanet_linear_gdr_gb300 import workloads as W
+    w = W.prefill()
+    pool = w.state_pool(w.live_slots())
+    init = torch.from_numpy(pool[w.slot_idx].view(np.int16)).to(dev).view(torch.bfloat16)
+    final = torch.empty_like(init)
+    qkv, dec, bet, off = (_to_dev(x, dev) for x in (w.qkv, w.decay, w.beta, w.offsets))
+    out = torch.empty((w.total_tokens, w.nv * w.V), device=dev)
+    a = gdr._binding.make_args(qkv, dec, bet, init, torch.zeros(w.batch, dtype=torch.int32, device=dev),
+                               off, out, nk=w.nk)
+    fn_c = gdr.load_library().gdr_fwd_dense
+    import ctypes
+
+    def fn():
+        gdr._binding._check(fn_c(ctypes.byref(a), init.data_ptr(), final.data_ptr(), stream.cuda_stream))
+    for _ in range(2):
+        fn()
+    ms = statistics.median(time_steps(fn, max(3, steps // 10), flush, stream))
+    ht = w.live_head_tokens
+    return {
+        "workload": f"ragged prefill, dense state: {w.batch} rows, T={w.total_tokens}, bf16 initial/final "
+                    f"[{w.batch},32,128,128]",
+        "ms": ms, "head_tokens_per_s": ht / (ms * 1e-3),
+        "frac_fp32_fma": fma_ops(ht, w.K, w.V) / (ms * 1e-3) / fp32_fma_peak(dev),
+    }
+
+
 def bench_verify_fold(dev, flush, stream, hbm_peak, steps, ring_dtype=None):
     """Speculative verify (bf16 pool, fp32 or bf16 ring of RING_LEN 8) then fold."""
     import torch
@@ -386,7 +419,7 @@ def bench_gdp_snapshots_beta_per_value(dev, flush, stream, hbm_peak, steps):
     return bench_gdp_snapshots(dev, flush, stream, hbm_peak, steps, beta_per_value=True)
 
 
-SECONDARY = {"prefill": bench_prefill, "verify_fold": bench_verify_fold,
+SECONDARY = {"prefill": bench_prefill, "prefill_dense": bench_prefill_dense, "verify_fold": bench_verify_fold,
              "verify_fold_bf16_ring": bench_verify_fold_bf16_ring,
              "gdp_snapshots": bench_gdp_snapshots,
              "gdp_snapshots_beta_per_value": bench_gdp_snapshots_beta_per_value}

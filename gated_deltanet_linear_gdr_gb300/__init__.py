@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     GdrError,
     gdr_fold,
     gdr_fwd,
+    gdr_fwd_dense,
     gdr_fwd_snapshots,
     gdr_get_status,
     gdr_output_shape,

@@ -80,6 +80,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                 "gdr_output_shape": ([i64, i32, i32, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
                 "gdr_ring_record_elements": ([i32, i32, i32], ctypes.c_int),
                 "gdr_fwd": ([A, vp], ctypes.c_int),
+                "gdr_fwd_dense": ([A, vp, vp, vp], ctypes.c_int),
                 "gdr_verify_ring": ([A, vp, i32, i64, i32, i64, vp, vp], ctypes.c_int),
                 "gdr_fold": ([A, vp, i32, i64, i32, i64, vp, vp, vp], ctypes.c_int),
                 "gdr_fwd_snapshots": ([A, vp, i64, i64, i64, i32, i32, vp], ctypes.c_int),
@@ -218,6 +219,37 @@ def gdr_fwd(qkv, decay, beta, state, slot_idx, offsets, out=None, *, decay_is_lo
                   max_row_len=max_row_len)
     _check(load_library().gdr_fwd(ctypes.byref(a), _stream(qkv.device)))
     return out
+
+
+def gdr_fwd_dense(qkv, decay, beta, offsets, initial_state=None, output_final_state=True, out=None, *,
+                  nv=None, K=None, state_dtype=torch.float32, decay_is_log=False, use_qk_l2norm=True,
+                  scale=0.0, eps=1e-6, max_row_len=0):
+    """Forward pass with a dense start / end state ("core.ssm.ops.gdp.fused_recurrent",
+    initial_state [N, HV, K, V] or None for zeros, output_final_state).  Returns
+    (out, final_state); final_state is a new [N, HV, K, V] tensor of the start
+    state's dtype (None unless output_final_state).  Without an initial state,
+    nv and K (= V) give the shape and state_dtype the dtype."""
+    batch = offsets.shape[0] - 1
+    if initial_state is not None:
+        ref = initial_state
+    else:
+        if nv is None or K is None:
+            raise ValueError("without initial_state, nv and K are needed")
+        ref = torch.empty((batch, nv, K, K), dtype=state_dtype, device=qkv.device)
+    final = torch.empty_like(ref, memory_format=torch.contiguous_format) if output_final_state else None
+    if initial_state is not None and final is not None and final.stride() != initial_state.stride():
+        raise ValueError("initial_state must be contiguous (final_state shares its strides)")
+    if out is None:
+        out = torch.empty(gdr_output_shape(qkv.shape[0], ref.shape[1], ref.shape[3]),
+                          dtype=torch.float32, device=qkv.device)
+    rows = torch.zeros(batch, dtype=torch.int32, device=qkv.device)  # shape only: not read
+    a = make_args(qkv, decay, beta, ref, rows, offsets, out, nk=_nk_from_qkv(qkv, ref),
+                  decay_is_log=decay_is_log, use_qk_l2norm=use_qk_l2norm, scale=scale, eps=eps,
+                  max_row_len=max_row_len)
+    _check(load_library().gdr_fwd_dense(
+        ctypes.byref(a), None if initial_state is None else initial_state.data_ptr(),
+        None if final is None else final.data_ptr(), _stream(qkv.device)))
+    return out, final
 
 
 def gdr_verify_ring(qkv, decay, beta, state, slot_idx, offsets, ring, ring_slot_idx, out=None, *,

@@ -150,6 +150,9 @@ gdr::StepParams lower(const gdr_step_args *a, unsigned *status) {
     p.offsets = a->offsets;
     p.qkv_vec = (a->qkv_chan_stride == 1 && aligned16(a->qkv) && a->qkv_seq_stride % 4 == 0) ? 1 : 0;
     p.out_vec = (a->out_vdim_stride == 1 && aligned16(a->out) && a->out_seq_stride % 4 == 0) ? 1 : 0;
+    p.state_in = a->state;
+    p.state_out = a->state;
+    p.dense = 0;
     p.status = status;
     return p;
 }
@@ -245,6 +248,36 @@ int gdr_fwd(const gdr_step_args *a, void *stream) {
     if (a->max_row_len == 1 && !p.bpv)
         return launched(gdr::launch_decode(p, a->K, a->state_dtype == GDR_BF16, s), "gdr_fwd");
     return launched(launch_rows(p, a, gdr::Mode::Fwd, gdr::RingParams{}, gdr::SnapParams{}, s), "gdr_fwd");
+}
+
+int gdr_fwd_dense(const gdr_step_args *a, const void *initial_state, void *final_state, void *stream) {
+    const char *fn = "gdr_fwd_dense";
+    if (!a) return fail(GDR_ERR_INVALID_ARG, "%s: args is NULL", fn);
+    // the dense buffers stand in for the pool: check them through a copy of the args
+    gdr_step_args d = *a;
+    d.state = initial_state ? const_cast<void *>(initial_state) : final_state;
+    d.max_slots = a->batch > 0 ? a->batch : 1;
+    static const int32_t kNoSlots = 0;
+    d.slot_idx = &kNoSlots;  // not read in the dense mode
+    int rc = check_step(&d, fn);
+    if (rc) return rc;
+    if (a->batch > 0 && !initial_state && !final_state)
+        return fail(GDR_ERR_INVALID_ARG, "%s: initial_state and final_state are both NULL", fn);
+    if ((initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)))
+        return fail(GDR_ERR_UNSUPPORTED, "%s: initial_state / final_state must be 16-byte aligned", fn);
+    if (a->batch == 0) return ok();
+    unsigned *st = nullptr;
+    if ((rc = status_ptr(&st))) return rc;
+    gdr::StepParams p = lower(&d, st);
+    p.state = nullptr;
+    p.slot_idx = nullptr;
+    p.state_in = initial_state;
+    p.state_out = final_state;
+    p.dense = 1;
+    const bool bf16 = a->state_dtype == GDR_BF16;
+    return launched(gdr::launch_chain(p, a->K, bf16, gdr::Mode::Fwd, gdr::RingParams{}, gdr::SnapParams{},
+                                      a->max_row_len, static_cast<cudaStream_t>(stream)),
+                    fn);
 }
 
 int gdr_verify_ring(const gdr_step_args *a, void *ring, int32_t ring_dtype, int64_t ring_rows,

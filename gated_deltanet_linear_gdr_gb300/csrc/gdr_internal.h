@@ -26,6 +26,12 @@ struct StepParams {
     long long st_slot, st_head, st_k;  // value-dim stride is 1
     long long max_slots;
     const int *slot_idx, *offsets;
+    // general kernel: rows read state_in (zeros if null) and commit to state_out
+    // (nothing if null); both equal `state` except in the dense mode, where
+    // row b uses slot b and every row is live (dense != 0)
+    const void *state_in;
+    void *state_out;
+    int dense;
     int bpv;      // beta per value element: element (t, h, j) at t*beta_ss + h*beta_hs + j*beta_vs
     long long beta_ss, beta_hs, beta_vs;
     int beta_vec; // per-element beta rows may be read with 16-byte vector loads

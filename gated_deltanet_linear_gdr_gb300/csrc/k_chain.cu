@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K, BPV, TCX>::NT, 4)
         return;
     }
     const int L = t1 - t0;
-    if (L == 0) return;
+    if (L == 0 && !p.dense) return;  // the dense mode still hands the start state on
     if (max_len > 0 && L > max_len) {
         if (leader) flag(p.status, GDR_STATUS_ROW_TOO_LONG);
         return;
@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(ChainShape<ST, K, BPV, TCX>::NT, 4)
     const int wcol = warp * WC + vl * C;           // lane's first column inside the slice
     const int col0 = slice * VS + wcol;            // ... inside the head
     float *obase = p.out + (long long)t0 * p.out_ss + (long long)(h * V + col0) * p.out_vs;
-    const int slot = p.slot_idx[b];
+    const int slot = p.dense ? b : p.slot_idx[b];
     if (slot < 0 || slot >= p.max_slots) {
         if (slot != -1 && leader) flag(p.status, GDR_STATUS_BAD_SLOT);
         if (kl == 0) {
@@ -114,14 +114,18 @@ __global__ void __launch_bounds__(ChainShape<ST, K, BPV, TCX>::NT, 4)
         }
     }
 
-    // State piece: rows kl*ROWS .. +ROWS, columns col0 .. col0+C.
-    ST *stile = reinterpret_cast<ST *>(p.state) + (long long)slot * p.st_slot +
-                (long long)h * p.st_head + (long long)(kl * ROWS) * p.st_k + col0;
+    // State piece: rows kl*ROWS .. +ROWS, columns col0 .. col0+C, read from
+    // state_in (zeros when null) and committed to state_out.
+    const long long soff = (long long)slot * p.st_slot + (long long)h * p.st_head + (long long)(kl * ROWS) * p.st_k + col0;
+    const ST *sin = p.state_in ? reinterpret_cast<const ST *>(p.state_in) + soff : nullptr;
     typename Sh::State s;
 #pragma unroll
     for (int i = 0; i < ROWS; ++i) {
         Pack<ST, C> x;
-        x.load(stile + i * p.st_k);
+        if (sin)
+            x.load(sin + i * p.st_k);
+        else
+            x.u.v = {};
 #pragma unroll
         for (int c = 0; c < C; ++c) s.set(i, c, x.get(c));
     }
@@ -279,13 +283,14 @@ __global__ void __launch_bounds__(ChainShape<ST, K, BPV, TCX>::NT, 4)
         if (overflow && leader) flag(p.status, GDR_STATUS_SNAPSHOT_OVERFLOW);
     }
     (void)records;
-    if (commit) {
+    if (commit && p.state_out) {
+        ST *sout = reinterpret_cast<ST *>(p.state_out) + soff;
 #pragma unroll
         for (int i = 0; i < ROWS; ++i) {
             Pack<ST, C> x;
 #pragma unroll
             for (int c = 0; c < C; ++c) x.set(c, s.get(i, c));
-            x.store(stile + i * p.st_k);
+            x.store(sout + i * p.st_k);
         }
     }
 }

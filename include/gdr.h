@@ -165,6 +165,18 @@ int gdr_ring_record_elements(int32_t K, int32_t V, int32_t ratio);
  * end).  Rows of length 0 leave their slot untouched. */
 int gdr_fwd(const gdr_step_args *args, void *stream);
 
+/* Forward pass with a dense start and end state ("core.ssm.ops.gdp.fused_recurrent",
+ * initial_state [N, HV, K, V] or None for zeros, output_final_state): as gdr_fwd,
+ * but row b starts from initial_state[b] (zeros when initial_state is NULL) and
+ * its final state is written to final_state[b] (nothing when NULL; at least one
+ * of the two must be given).  Both are [batch, nv, K, V] in state_dtype with
+ * the args' state strides (state_slot_stride steps between rows) and 16-byte
+ * alignment.  args->state, slot_idx and max_slots are ignored; every row is
+ * live, and an empty row writes its start state to final_state.  The buffers
+ * may be the same (in-place update). */
+int gdr_fwd_dense(const gdr_step_args *args, const void *initial_state, void *final_state,
+                  void *stream);
+
 /* Verify pass ("gated_delta_recurrence_verify_ring_gpu", summary): writes the
  * same out as gdr_fwd and leaves the pool untouched, except that a row longer
  * than ring_len records nothing and commits its state exactly as gdr_fwd does.

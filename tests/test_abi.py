@@ -170,6 +170,18 @@ def test_verify_and_fold_reject_bad_ring(lib):
         B.GDR_ERR_INVALID_ARG  # ring_rows 0
 
 
+def test_fwd_dense_rejects_bad_buffers(lib):
+    a = _valid_args()
+    a.state = a.slot_idx = None  # ignored by the dense entry point
+    a.max_slots = 0
+    fake = 0x7f0000000000
+    assert lib.gdr_fwd_dense(ctypes.byref(a), None, None, None) == B.GDR_ERR_INVALID_ARG
+    assert lib.gdr_fwd_dense(ctypes.byref(a), fake + 8, None, None) == B.GDR_ERR_UNSUPPORTED
+    assert lib.gdr_fwd_dense(ctypes.byref(a), fake, fake + 8, None) == B.GDR_ERR_UNSUPPORTED
+    a.V = 32  # K != V, as for every entry point
+    assert lib.gdr_fwd_dense(ctypes.byref(a), fake, fake, None) == B.GDR_ERR_UNSUPPORTED
+
+
 def test_verify_rejects_per_element_beta(lib):
     a = _valid_args()
     a.V = a.K = 16

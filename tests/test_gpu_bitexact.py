@@ -6,6 +6,7 @@ over the draft prefix; and the library's own guarantees (kernel choice,
 batch composition, strides and repeated runs do not change any bit)."""
 from __future__ import annotations
 
+import ctypes
 import dataclasses
 
 import numpy as np
@@ -57,6 +58,30 @@ def test_verify_output_equals_forward_and_pool_untouched(state_dtype):
             assert torch.isnan(ring[int(w.ring_slot_idx[b])]).all(), "long row must not record"
         else:
             assert (host[s] == pool[s]).all(), "verify must leave the pool alone"
+
+
+@pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
+def test_dense_state_equals_pool_at_the_rows_slots(state_dtype):
+    """The dense mode is the slot-indexed pass with the rows' states gathered:
+    same output bits, final[b] = the pool slot of row b after the pass; also
+    when the start and end buffers are the same tensor."""
+    w = W.random_case(710, [17, 3, 1, 33], nk=2, nv=4, K=128, max_slots=9, state_dtype=state_dtype)
+    pool = w.state_pool()
+    out_pool, pool_after = _run_fwd(w, pool)
+    init = pool_to_dev(pool[w.slot_idx])
+    d = Dev(w, pool)
+    out, final = gdr.gdr_fwd_dense(d.qkv, d.decay, d.beta, d.off, init)
+    torch.cuda.synchronize()
+    assert (out.cpu().numpy().view(np.uint32) == out_pool.view(np.uint32)).all()
+    assert (pool_to_host(final) == pool_after[w.slot_idx]).all()
+    # in place: one buffer as start and end state, through the C entry point
+    a = gdr._binding.make_args(d.qkv, d.decay, d.beta, init, torch.zeros(w.batch, dtype=torch.int32,
+                               device=DEV), d.off, out, nk=w.nk)
+    gdr._binding._check(gdr.load_library().gdr_fwd_dense(
+        ctypes.byref(a), init.data_ptr(), init.data_ptr(), torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert (pool_to_host(init) == pool_after[w.slot_idx]).all()
+    assert (out.cpu().numpy().view(np.uint32) == out_pool.view(np.uint32)).all()
 
 
 @pytest.mark.parametrize("state_dtype", ["bf16", "f32"])

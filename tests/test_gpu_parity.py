@@ -179,6 +179,32 @@ def test_fold_on_synthetic_ring(state_dtype):
             assert (host[s] == pool[s]).all()
 
 
+@pytest.mark.parametrize("K", [16, 64, 128])
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("with_initial", [True, False])
+def test_dense_state_forward(K, state_dtype, with_initial):
+    """initial_state / output_final_state ("core.ssm.ops.gdp.fused_recurrent")
+    against the oracle: ragged rows, an empty row (its final state is its start
+    state), with and without a start state."""
+    w = W.random_case(700 + K, [21, 0, 5, 1], nk=2, nv=4, K=K, max_slots=4, state_dtype=state_dtype)
+    init = w.state_pool()[np.arange(w.batch)] if with_initial else None
+    kw = dict(nk=w.nk, nv=w.nv, K=w.K, V=w.V, state_dtype=state_dtype, decay_is_log=w.decay_is_log,
+              use_l2norm=w.use_l2norm, scale=w.scale, eps=w.eps)
+    ref_out, ref_final = oracle.fwd_dense(w.qkv, w.decay, w.beta, w.offsets, init, **kw)
+    tdt = torch.bfloat16 if state_dtype == "bf16" else torch.float32
+    out, final = gdr.gdr_fwd_dense(
+        torch.from_numpy(w.qkv).to(DEV), torch.from_numpy(w.decay).to(DEV),
+        torch.from_numpy(w.beta).to(DEV), torch.from_numpy(w.offsets).to(DEV),
+        None if init is None else pool_to_dev(init), nv=w.nv, K=w.K, state_dtype=tdt)
+    torch.cuda.synchronize()
+    check_out(out, ref_out)
+    check_state(pool_to_host(final), ref_final)
+    if init is not None:
+        assert (pool_to_host(final)[1] == init[1]).all(), "an empty row hands its start state on"
+    else:
+        assert (as_f64(pool_to_host(final)[1]) == 0).all()
+
+
 @pytest.mark.parametrize("K", [16, 32, 64, 128])
 @pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("hint", [0, 1, 40])

@@ -206,11 +206,11 @@ def gdp_snapshots(seed: int = 4, batch: int = 64, drafts: int = 4, householder: 
 def random_case(seed: int, lengths, nk: int, nv: int, K: int, max_slots: int,
                 state_dtype: str = "f32", n_pad: int = 0, decay_is_log: bool = False,
                 use_l2norm: bool = True, scale: float = 0.0, state_std: float = 0.1,
-                beta_per_value: bool = False) -> Workload:
+                beta_per_value: bool = False, V: int = 0) -> Workload:
     """A small general case for parity tests: given row lengths, random slots;
-    beta per value element when beta_per_value."""
+    beta per value element when beta_per_value; value head size V (K if 0)."""
     rng = np.random.default_rng(seed)
-    V = K
+    V = V or K
     L = np.asarray(lengths, dtype=np.int64)
     batch = len(L)
     offsets = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)

@@ -77,6 +77,40 @@ def test_matches_matrix_form_bruteforce(use_l2norm, decay_is_log):
         np.testing.assert_array_equal(p.state[slot, h], S.astype(np.float32))
 
 
+@pytest.mark.parametrize("KV", [(4, 8), (8, 4)])
+def test_matches_matrix_form_bruteforce_k_ne_v(KV):
+    """K != V ("core.ssm.ops.gdp.fused_recurrent": K and V are separate sizes)."""
+    K, V = KV
+    w = _small(14, [3, 4], nk=1, nv=2, K=K, V=V)
+    pool = w.state_pool()
+    p = problem(w, state=pool.copy())
+    out = oracle.fwd(p)
+    ref_out, finals = brute.fwd(w.qkv, w.decay, w.beta, pool, w.slot_idx, w.offsets,
+                                nk=w.nk, nv=w.nv, K=K, V=V, eps=w.eps)
+    np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-12)
+    for (s, h), S in finals.items():
+        np.testing.assert_allclose(p.state[s, h], S, rtol=1e-6, atol=1e-7)
+
+
+def test_value_columns_split_into_independent_halves():
+    """The value columns never mix: a V = 2K run equals, exactly, two V = K runs
+    on the two halves of the value columns (v, state and output split alike)."""
+    K = 16
+    w = _small(15, [5, 2], nk=1, nv=2, K=K, V=2 * K, state_dtype="f32")
+    pool = w.state_pool()
+    p = problem(w, state=pool.copy())
+    out = oracle.fwd(p)
+    nv, qk = w.nv, 2 * w.nk * K
+    for half in range(2):
+        cols = slice(half * K, (half + 1) * K)
+        v = w.qkv[:, qk:].reshape(-1, nv, 2 * K)[:, :, cols].reshape(-1, nv * K)
+        wh = dataclasses.replace(w, V=K, qkv=np.concatenate([w.qkv[:, :qk], v], axis=1))
+        ph = problem(wh, state=np.ascontiguousarray(pool[..., cols]))
+        out_h = oracle.fwd(ph)
+        assert (out.reshape(-1, nv, 2 * K)[:, :, cols] == out_h.reshape(-1, nv, K)).all()
+        assert (p.state[..., cols] == ph.state).all()
+
+
 def test_tiny_config_matches_bruteforce():
     w = W.tiny()
     pool = w.state_pool()

@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--impl", default="gdr", choices=["gdr", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "prefill_dense", "verify_fold", "verify_fold_bf16_ring",
+    ap.add_argument("--only", choices=["prefill", "prefill_dense", "prefill_v2k", "verify_fold", "verify_fold_bf16_ring",
                                        "gdp_snapshots",
                                        "gdp_snapshots_beta_per_value"],
                     default=None,
@@ -260,12 +260,12 @@ def _pool_dev(w, dev):
     return torch.from_numpy(pool).to(dev)
 
 
-def bench_prefill(dev, flush, stream, hbm_peak, steps):
+def bench_prefill(dev, flush, stream, hbm_peak, steps, V=0):
     """Ragged prefill (FP32-FMA bound): rows of 512..4096 tokens."""
     import torch
     import gated_deltanet_linear_gdr_gb300 as gdr
     from gated_deltanet_linear_gdr_gb300 import workloads as W
-    w = W.prefill()
+    w = W.prefill(V=V)
     st = _pool_dev(w, dev)
     qkv, dec, bet, slot, off = (_to_dev(x, dev) for x in (w.qkv, w.decay, w.beta, w.slot_idx, w.offsets))
     out = torch.empty((w.total_tokens, w.nv * w.V), device=dev)
@@ -277,13 +277,18 @@ def bench_prefill(dev, flush, stream, hbm_peak, steps):
     fp32_peak = fp32_fma_peak(dev)
     return {
         "workload": f"ragged prefill: {w.batch} rows, lengths {w.row_lengths.min()}..{w.row_lengths.max()}"
-                    f" (T={w.total_tokens}), nk=16, nv=32, K=V=128, bf16 pool [16,32,128,128]",
+                    f" (T={w.total_tokens}), nk=16, nv=32, K={w.K}, V={w.V}, bf16 pool [16,32,{w.K},{w.V}]",
         "ms": ms, "head_tokens_per_s": ht / (ms * 1e-3),
         "fma_tflops_equiv": fma_ops(ht, w.K, w.V) / (ms * 1e-3) / 1e12,
         "fp32_fma_peak_tops": fp32_peak / 1e12,
         "frac_fp32_fma": fma_ops(ht, w.K, w.V) / (ms * 1e-3) / fp32_peak,
         "hbm_gbs": decode_bytes(w, 2) / (ms * 1e-3) / 1e9,
     }
+
+
+def bench_prefill_v2k(dev, flush, stream, hbm_peak, steps):
+    """The ragged prefill workload with value heads twice the key heads (V = 256)."""
+    return bench_prefill(dev, flush, stream, hbm_peak, steps, V=256)
 
 
 def bench_prefill_dense(dev, flush, stream, hbm_peak, steps):
@@ -419,7 +424,8 @@ def bench_gdp_snapshots_beta_per_value(dev, flush, stream, hbm_peak, steps):
     return bench_gdp_snapshots(dev, flush, stream, hbm_peak, steps, beta_per_value=True)
 
 
-SECONDARY = {"prefill": bench_prefill, "prefill_dense": bench_prefill_dense, "verify_fold": bench_verify_fold,
+SECONDARY = {"prefill": bench_prefill, "prefill_dense": bench_prefill_dense, "prefill_v2k": bench_prefill_v2k,
+             "verify_fold": bench_verify_fold,
              "verify_fold_bf16_ring": bench_verify_fold_bf16_ring,
              "gdp_snapshots": bench_gdp_snapshots,
              "gdp_snapshots_beta_per_value": bench_gdp_snapshots_beta_per_value}

@@ -68,9 +68,8 @@ int check_pool(const gdr_step_args *a, const char *fn) {
         return fail(GDR_ERR_INVALID_ARG, "%s: nv=%d, nk=%d must be positive", fn, a->nv, a->nk);
     if (a->nv % a->nk != 0)
         return fail(GDR_ERR_INVALID_ARG, "%s: nv=%d is not a multiple of nk=%d", fn, a->nv, a->nk);
-    if (a->K != a->V)
-        return fail(GDR_ERR_UNSUPPORTED, "%s: K=%d != V=%d (value head dim must equal key head dim)",
-                    fn, a->K, a->V);
+    if (a->V != a->K && a->V != 2 * a->K)
+        return fail(GDR_ERR_UNSUPPORTED, "%s: V=%d must be K=%d or 2K", fn, a->V, a->K);
     if (!supported_dim(a->K))
         return fail(GDR_ERR_UNSUPPORTED, "%s: K=%d not in {16,32,64,128}", fn, a->K);
     if (a->state_dtype != GDR_F32 && a->state_dtype != GDR_BF16)
@@ -167,12 +166,12 @@ constexpr long long kShortRowMax = 64;
 cudaError_t launch_rows(const gdr::StepParams &p, const gdr_step_args *a, gdr::Mode mode, const gdr::RingParams &rp,
                         const gdr::SnapParams &sp, cudaStream_t s) {
     const bool bf16 = a->state_dtype == GDR_BF16;
-    if (!p.bpv && mode != gdr::Mode::Snap && a->max_row_len >= 1 && a->max_row_len <= kShortRowMax) {
+    if (!p.bpv && a->V == a->K && mode != gdr::Mode::Snap && a->max_row_len >= 1 && a->max_row_len <= kShortRowMax) {
         bool used = false;
         cudaError_t e = gdr::launch_short(p, a->K, bf16, mode, rp, sp, a->max_row_len, s, &used);
         if (used || e != cudaSuccess) return e;
     }
-    return gdr::launch_chain(p, a->K, bf16, mode, rp, sp, a->max_row_len, s);
+    return gdr::launch_chain(p, a->K, a->V, bf16, mode, rp, sp, a->max_row_len, s);
 }
 
 int launched(cudaError_t e, const char *fn) {
@@ -245,7 +244,7 @@ int gdr_fwd(const gdr_step_args *a, void *stream) {
     if ((rc = status_ptr(&st))) return rc;
     const gdr::StepParams p = lower(a, st);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (a->max_row_len == 1 && !p.bpv)
+    if (a->max_row_len == 1 && !p.bpv && a->V == a->K)
         return launched(gdr::launch_decode(p, a->K, a->state_dtype == GDR_BF16, s), "gdr_fwd");
     return launched(launch_rows(p, a, gdr::Mode::Fwd, gdr::RingParams{}, gdr::SnapParams{}, s), "gdr_fwd");
 }
@@ -275,7 +274,7 @@ int gdr_fwd_dense(const gdr_step_args *a, const void *initial_state, void *final
     p.state_out = final_state;
     p.dense = 1;
     const bool bf16 = a->state_dtype == GDR_BF16;
-    return launched(gdr::launch_chain(p, a->K, bf16, gdr::Mode::Fwd, gdr::RingParams{}, gdr::SnapParams{},
+    return launched(gdr::launch_chain(p, a->K, a->V, bf16, gdr::Mode::Fwd, gdr::RingParams{}, gdr::SnapParams{},
                                       a->max_row_len, static_cast<cudaStream_t>(stream)),
                     fn);
 }
@@ -286,6 +285,8 @@ int gdr_verify_ring(const gdr_step_args *a, void *ring, int32_t ring_dtype, int6
     if (rc) return rc;
     if (a->beta_vdim_stride > 0)
         return fail(GDR_ERR_UNSUPPORTED, "gdr_verify_ring: beta must be [total_tokens, nv] (beta_vdim_stride 0)");
+    if (a->V != a->K)
+        return fail(GDR_ERR_UNSUPPORTED, "gdr_verify_ring: V=%d must equal K=%d", a->V, a->K);
     const int r = a->nv / a->nk;
     rc = check_ring(ring_dtype, ring_rows, ring_len, record_stride, ring, ring_slot_idx, a->K, a->V, r,
                     a->batch, true, "gdr_verify_ring");
@@ -311,6 +312,7 @@ int gdr_fold(const gdr_step_args *a, const void *ring, int32_t ring_dtype, int64
              int64_t record_stride, const int32_t *ring_slot_idx, const int32_t *counts, void *stream) {
     int rc = check_pool(a, "gdr_fold");
     if (rc) return rc;
+    if (a->V != a->K) return fail(GDR_ERR_UNSUPPORTED, "gdr_fold: V=%d must equal K=%d", a->V, a->K);
     const int r = a->nv / a->nk;
     rc = check_ring(ring_dtype, ring_rows, ring_len, record_stride, ring, ring_slot_idx, a->K, a->V, r,
                     a->batch, false, "gdr_fold");
@@ -393,7 +395,7 @@ int gdr_rollback(const gdr_step_args *a, const void *inter, int64_t inter_slot_s
     p.n_inter = n_inter;
     p.accepted = accepted;
     p.status = st;
-    return launched(gdr::launch_rollback(p, a->K, a->state_dtype == GDR_BF16, static_cast<cudaStream_t>(stream)),
+    return launched(gdr::launch_rollback(p, a->K, a->V, a->state_dtype == GDR_BF16, static_cast<cudaStream_t>(stream)),
                     "gdr_rollback");
 }
 

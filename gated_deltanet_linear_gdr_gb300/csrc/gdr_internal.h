@@ -113,13 +113,13 @@ struct FastDiv {
 
 // Launchers (defined next to their kernels).  Return cudaGetLastError().
 cudaError_t launch_decode(const StepParams &p, int K, bool bf16, cudaStream_t s);
-cudaError_t launch_chain(const StepParams &p, int K, bool bf16, Mode mode, const RingParams &rp,
+cudaError_t launch_chain(const StepParams &p, int K, int V, bool bf16, Mode mode, const RingParams &rp,
                          const SnapParams &sp, long long max_row_len, cudaStream_t s);
 // Pipelined short-row kernel; sets *used = false (launching nothing) when the
 // layout does not allow it, so the caller falls back to launch_chain.
 cudaError_t launch_short(const StepParams &p, int K, bool bf16, Mode mode, const RingParams &rp,
                          const SnapParams &sp, long long max_row_len, cudaStream_t s, bool *used);
 cudaError_t launch_fold(const FoldParams &p, int K, bool bf16, cudaStream_t s);
-cudaError_t launch_rollback(const RollbackParams &p, int K, bool bf16, cudaStream_t s);
+cudaError_t launch_rollback(const RollbackParams &p, int K, int V, bool bf16, cudaStream_t s);
 
 }  // namespace gdr

@@ -24,8 +24,8 @@ namespace gdr {
 // short (a smaller stage, so more L1 is left) and for per-element beta (BPV:
 // beta staged per token like v; 8 tokens keep the static shared memory under
 // 48 KiB).
-template <typename ST, int K, bool BPV = false, int TCX = 16> struct ChainShape {
-    static constexpr int V = K;
+template <typename ST, int K, int VV = K, bool BPV = false, int TCX = 16> struct ChainShape {
+    static constexpr int V = VV;                   // value head size: K or 2K
     static constexpr int NG = K / 8;               // row groups
     static constexpr int LK = NG >= 4 ? cmin(4, NG / 2) : NG;  // lanes along K
     static constexpr int RG = NG / LK;             // groups per lane
@@ -48,11 +48,11 @@ template <typename ST, int K, bool BPV = false, int TCX = 16> struct ChainShape 
 // Shared-memory index of raw row i (natural order, padded every ROWS rows).
 template <int ROWS> __device__ __forceinline__ int pidx(int i) { return vpos<false, ROWS>(i); }
 
-template <typename ST, int K, Mode MODE, bool BPV, int TCX>
-__global__ void __launch_bounds__(ChainShape<ST, K, BPV, TCX>::NT, 4)
+template <typename ST, int K, int VV, Mode MODE, bool BPV, int TCX>
+__global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX>::NT, 4)
     k_chain(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len) {
-    using Sh = ChainShape<ST, K, BPV, TCX>;
-    constexpr int V = K, LK = Sh::LK, ROWS = Sh::ROWS, C = Sh::C;
+    using Sh = ChainShape<ST, K, VV, BPV, TCX>;
+    constexpr int V = VV, LK = Sh::LK, ROWS = Sh::ROWS, C = Sh::C;
     constexpr int WC = Sh::WC, W = Sh::W, NT = Sh::NT, VS = Sh::VS, SLICES = Sh::SLICES;
     constexpr int KP = Sh::KP, TC = Sh::TC, NL = Sh::NL, TPW = Sh::TPW;
 
@@ -295,11 +295,11 @@ __global__ void __launch_bounds__(ChainShape<ST, K, BPV, TCX>::NT, 4)
     }
 }
 
-template <typename ST, int K>
+template <typename ST, int K, int V>
 static cudaError_t launch_chain_t(const StepParams &p, Mode mode, const RingParams &rp,
                                   const SnapParams &sp, long long max_len, cudaStream_t st) {
-    using Sh = ChainShape<ST, K>;
-    static_assert(ChainShape<ST, K, true>::SLICES == Sh::SLICES && ChainShape<ST, K, true>::NT == Sh::NT,
+    using Sh = ChainShape<ST, K, V>;
+    static_assert(ChainShape<ST, K, V, true>::SLICES == Sh::SLICES && ChainShape<ST, K, V, true>::NT == Sh::NT,
                   "same grid with per-element beta");
     const long long blocks = (long long)p.batch * p.nv * Sh::SLICES;
     if (blocks <= 0) return cudaGetLastError();
@@ -307,32 +307,41 @@ static cudaError_t launch_chain_t(const StepParams &p, Mode mode, const RingPara
     switch (mode) {
         case Mode::Fwd:
             if (p.bpv)
-                k_chain<ST, K, Mode::Fwd, true, 8><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+                k_chain<ST, K, V, Mode::Fwd, true, 8><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             else
-                k_chain<ST, K, Mode::Fwd, false, 16><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+                k_chain<ST, K, V, Mode::Fwd, false, 16><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             break;
-        case Mode::Verify:  // head-wise beta only
-            if (p.bpv) return cudaErrorInvalidValue;
-            k_chain<ST, K, Mode::Verify, false, 16><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+        case Mode::Verify:  // head-wise beta and V == K only
+            if constexpr (V == K) {
+                if (p.bpv) return cudaErrorInvalidValue;
+                k_chain<ST, K, V, Mode::Verify, false, 16><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+            } else {
+                return cudaErrorInvalidValue;
+            }
             break;
         case Mode::Snap:
             if (p.bpv)
-                k_chain<ST, K, Mode::Snap, true, 8><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+                k_chain<ST, K, V, Mode::Snap, true, 8><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             else if (short_rows)
-                k_chain<ST, K, Mode::Snap, false, 8><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+                k_chain<ST, K, V, Mode::Snap, false, 8><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             else
-                k_chain<ST, K, Mode::Snap, false, 16><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
+                k_chain<ST, K, V, Mode::Snap, false, 16><<<(unsigned)blocks, Sh::NT, 0, st>>>(p, rp, sp, max_len);
             break;
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_chain(const StepParams &p, int K, bool bf16, Mode mode, const RingParams &rp,
+cudaError_t launch_chain(const StepParams &p, int K, int V, bool bf16, Mode mode, const RingParams &rp,
                          const SnapParams &sp, long long max_row_len, cudaStream_t s) {
-#define GDR_CASE(KK)                                                                    \
-    case KK:                                                                            \
-        return bf16 ? launch_chain_t<uint16_t, KK>(p, mode, rp, sp, max_row_len, s)     \
-                    : launch_chain_t<float, KK>(p, mode, rp, sp, max_row_len, s);
+#define GDR_CASE(KK)                                                                                   \
+    case KK:                                                                                           \
+        if (V == KK)                                                                                   \
+            return bf16 ? launch_chain_t<uint16_t, KK, KK>(p, mode, rp, sp, max_row_len, s)            \
+                        : launch_chain_t<float, KK, KK>(p, mode, rp, sp, max_row_len, s);              \
+        if (V == 2 * KK)                                                                               \
+            return bf16 ? launch_chain_t<uint16_t, KK, 2 * KK>(p, mode, rp, sp, max_row_len, s)        \
+                        : launch_chain_t<float, KK, 2 * KK>(p, mode, rp, sp, max_row_len, s);          \
+        return cudaErrorInvalidValue;
     switch (K) {
         GDR_CASE(16)
         GDR_CASE(32)

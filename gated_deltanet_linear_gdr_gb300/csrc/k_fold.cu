@@ -18,8 +18,8 @@ namespace gdr {
 
 constexpr int kFoldThreads = 256;
 
-template <typename ST, int K> struct FoldShape {
-    static constexpr int V = K;
+template <typename ST, int K, int VV = K> struct FoldShape {
+    static constexpr int V = VV;
     static constexpr int CF = cmin(16 / (int)sizeof(ST), V);  // columns per thread (16 B)
     static constexpr int LVF = V / CF;                         // threads along a row
     static constexpr int RPP = kFoldThreads / LVF;             // rows per pass of the CTA
@@ -141,10 +141,10 @@ __global__ void __launch_bounds__(kFoldThreads) k_fold(const FoldParams p) {
     }
 }
 
-template <typename ST, int K>
+template <typename ST, int K, int VV>
 __global__ void __launch_bounds__(kFoldThreads) k_rollback(const RollbackParams p) {
-    using Sh = FoldShape<ST, K>;
-    constexpr int V = K, CF = Sh::CF, LVF = Sh::LVF, RPP = Sh::RPP, RB = Sh::RB, BLOCKS = Sh::BLOCKS;
+    using Sh = FoldShape<ST, K, VV>;
+    constexpr int V = VV, CF = Sh::CF, LVF = Sh::LVF, RPP = Sh::RPP, RB = Sh::RB, BLOCKS = Sh::BLOCKS;
     const int tid = threadIdx.x;
     const int blk = (int)(blockIdx.x % BLOCKS);
     const long long bh = blockIdx.x / BLOCKS;
@@ -290,9 +290,9 @@ template <typename ST, int K, typename RT> static cudaError_t launch_fold_t(cons
     return cudaGetLastError();
 }
 
-template <typename ST, int K> static cudaError_t launch_rollback_t(const RollbackParams &p, cudaStream_t st) {
-    const long long blocks = (long long)p.batch * p.nv * FoldShape<ST, K>::BLOCKS;
-    if (blocks > 0) k_rollback<ST, K><<<(unsigned)blocks, kFoldThreads, 0, st>>>(p);
+template <typename ST, int K, int V> static cudaError_t launch_rollback_t(const RollbackParams &p, cudaStream_t st) {
+    const long long blocks = (long long)p.batch * p.nv * FoldShape<ST, K, V>::BLOCKS;
+    if (blocks > 0) k_rollback<ST, K, V><<<(unsigned)blocks, kFoldThreads, 0, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -324,10 +324,13 @@ cudaError_t launch_fold(const FoldParams &p, int K, bool bf16, cudaStream_t s) {
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_rollback(const RollbackParams &p, int K, bool bf16, cudaStream_t s) {
-#define GDR_CASE(KK)                                                                            \
-    case KK:                                                                                    \
-        return bf16 ? launch_rollback_t<uint16_t, KK>(p, s) : launch_rollback_t<float, KK>(p, s);
+cudaError_t launch_rollback(const RollbackParams &p, int K, int V, bool bf16, cudaStream_t s) {
+#define GDR_CASE(KK)                                                                                      \
+    case KK:                                                                                              \
+        if (V == KK) return bf16 ? launch_rollback_t<uint16_t, KK, KK>(p, s) : launch_rollback_t<float, KK, KK>(p, s); \
+        if (V == 2 * KK)                                                                                  \
+            return bf16 ? launch_rollback_t<uint16_t, KK, 2 * KK>(p, s) : launch_rollback_t<float, KK, 2 * KK>(p, s); \
+        return cudaErrorInvalidValue;
     switch (K) {
         GDR_CASE(16)
         GDR_CASE(32)

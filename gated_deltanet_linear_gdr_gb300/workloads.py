@@ -137,10 +137,11 @@ def decode(seed: int = 1, batch: int = 256, max_slots: int = 512, n_pad: int = 8
 
 def prefill(seed: int = 2, batch: int = 8, max_slots: int = 16, lmin: int = 512,
             lmax: int = 4096, nk: int = 16, nv: int = 32, K: int = 128,
-            state_dtype: str = "bf16", lengths=None) -> Workload:
-    """Ragged rows with lengths ~ U{lmin..lmax}; the pool is read and written in place."""
+            state_dtype: str = "bf16", lengths=None, V: int = 0) -> Workload:
+    """Ragged rows with lengths ~ U{lmin..lmax}; the pool is read and written in
+    place; value head size V (K if 0)."""
     rng = np.random.default_rng(seed)
-    V = K
+    V = V or K
     L = (np.asarray(lengths, dtype=np.int64) if lengths is not None
          else rng.integers(lmin, lmax + 1, size=batch))
     batch = len(L)

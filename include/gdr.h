@@ -39,6 +39,10 @@
  *     library picks: every pass uses one fixed order of float32 operations per
  *     (row, head), so the same row gives the same bits in any call.
  *   - Two live rows of one call must not share a pool slot (they would race).
+ *   - Head sizes: K in {16, 32, 64, 128}; V = K, or V = 2K for the forward,
+ *     dense and snapshot passes and rollback ("core.ssm.ops.gdp.fused_recurrent"
+ *     sizes K and V separately; the verify ring and fold need V = K, as
+ *     "gated_delta_recurrence_verify_ring_gpu" requires).
  */
 #ifndef GDR_H
 #define GDR_H
@@ -52,7 +56,7 @@ extern "C" {
 /* ---- return codes ------------------------------------------------------- */
 #define GDR_OK 0
 #define GDR_ERR_INVALID_ARG (-1) /* null pointer, negative size, nv % nk != 0, bad stride */
-#define GDR_ERR_UNSUPPORTED (-2) /* K != V, K not in {16,32,64,128}, dtype, misalignment  */
+#define GDR_ERR_UNSUPPORTED (-2) /* head sizes, dtype, misalignment, unsupported mode      */
 #define GDR_ERR_CUDA (-3)        /* a CUDA call or kernel launch failed                   */
 
 /* ---- device status bits (sticky until cleared by gdr_get_status) -------- */

@@ -98,7 +98,7 @@ def _valid_args():
 
 
 BAD = [
-    ("K != V", lambda a: setattr(a, "V", 32), B.GDR_ERR_UNSUPPORTED),
+    ("V not K or 2K", lambda a: setattr(a, "V", 48), B.GDR_ERR_UNSUPPORTED),
     ("K unsupported", lambda a: (setattr(a, "K", 48), setattr(a, "V", 48)), B.GDR_ERR_UNSUPPORTED),
     ("nv % nk", lambda a: setattr(a, "nk", 3), B.GDR_ERR_INVALID_ARG),
     ("nv <= 0", lambda a: setattr(a, "nv", 0), B.GDR_ERR_INVALID_ARG),
@@ -170,6 +170,18 @@ def test_verify_and_fold_reject_bad_ring(lib):
         B.GDR_ERR_INVALID_ARG  # ring_rows 0
 
 
+def test_verify_and_fold_need_v_equal_k(lib):
+    a = _valid_args()
+    a.V = 32  # 2K: fine for the forward pass, not for the ring
+    a.state_dtype = B.GDR_F32
+    fake = 0x7f0000000000
+    need = lib.gdr_ring_record_elements(16, 32, 2)
+    assert lib.gdr_verify_ring(ctypes.byref(a), fake, B.GDR_F32, 4, 8, need, fake, None) == \
+        B.GDR_ERR_UNSUPPORTED
+    assert lib.gdr_fold(ctypes.byref(a), fake, B.GDR_F32, 4, 8, need, fake, fake, None) == \
+        B.GDR_ERR_UNSUPPORTED
+
+
 def test_fwd_dense_rejects_bad_buffers(lib):
     a = _valid_args()
     a.state = a.slot_idx = None  # ignored by the dense entry point
@@ -178,7 +190,7 @@ def test_fwd_dense_rejects_bad_buffers(lib):
     assert lib.gdr_fwd_dense(ctypes.byref(a), None, None, None) == B.GDR_ERR_INVALID_ARG
     assert lib.gdr_fwd_dense(ctypes.byref(a), fake + 8, None, None) == B.GDR_ERR_UNSUPPORTED
     assert lib.gdr_fwd_dense(ctypes.byref(a), fake, fake + 8, None) == B.GDR_ERR_UNSUPPORTED
-    a.V = 32  # K != V, as for every entry point
+    a.V = 48  # V neither K nor 2K, as for every entry point
     assert lib.gdr_fwd_dense(ctypes.byref(a), fake, fake, None) == B.GDR_ERR_UNSUPPORTED
 
 

@@ -61,6 +61,25 @@ def test_verify_output_equals_forward_and_pool_untouched(state_dtype):
 
 
 @pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
+def test_value_head_twice_key_head_equals_two_halves(state_dtype):
+    """The value columns never mix: a V = 2K pass gives, bit for bit, the two
+    V = K passes on the halves of the value columns."""
+    K = 128
+    w = W.random_case(820, [19, 2, 1], nk=2, nv=4, K=K, V=2 * K, max_slots=6, state_dtype=state_dtype)
+    pool = w.state_pool()
+    out, after = _run_fwd(w, pool)
+    nv, qk = w.nv, 2 * w.nk * K
+    for half in range(2):
+        cols = slice(half * K, (half + 1) * K)
+        v = w.qkv[:, qk:].reshape(-1, nv, 2 * K)[:, :, cols].reshape(-1, nv * K)
+        wh = dataclasses.replace(w, V=K, qkv=np.ascontiguousarray(np.concatenate([w.qkv[:, :qk], v], axis=1)))
+        out_h, after_h = _run_fwd(wh, np.ascontiguousarray(pool[..., cols]))
+        assert (out.reshape(-1, nv, 2 * K)[:, :, cols].view(np.uint32) ==
+                out_h.reshape(-1, nv, K).view(np.uint32)).all()
+        assert (after[..., cols] == after_h).all()
+
+
+@pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
 def test_dense_state_equals_pool_at_the_rows_slots(state_dtype):
     """The dense mode is the slot-indexed pass with the rows' states gathered:
     same output bits, final[b] = the pool slot of row b after the pass; also

@@ -181,6 +181,50 @@ def test_fold_on_synthetic_ring(state_dtype):
 
 @pytest.mark.parametrize("K", [16, 64, 128])
 @pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("hint", [0, 1])
+def test_value_head_twice_key_head_forward(K, state_dtype, hint):
+    """V = 2K ("core.ssm.ops.gdp.fused_recurrent": K and V sized separately)
+    against the oracle, ragged rows with a padding row."""
+    lengths = [1, 18, 0, 7] if hint == 0 else [1, 1, 1, 0]
+    w = W.random_case(800 + K, lengths, nk=2, nv=4, K=K, V=2 * K, max_slots=9, state_dtype=state_dtype,
+                      n_pad=1)
+    _fwd_parity(w, max_row_len=hint)
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_value_head_twice_key_head_snapshots_rollback_dense(state_dtype):
+    w = W.random_case(810, [8, 6, 8], nk=2, nv=4, K=64, V=128, max_slots=6, state_dtype=state_dtype,
+                      decay_is_log=True)
+    pool = w.state_pool()
+    d = Dev(w, pool)
+    tdt = torch.bfloat16 if state_dtype == "bf16" else torch.float32
+    inter = torch.zeros((w.max_slots, 4, w.nv, w.K, w.V), dtype=tdt, device=DEV)
+    out = d.snapshots(inter, 2)
+    torch.cuda.synchronize()
+    p = problem(w, state=pool.copy())
+    oint = np.zeros(tuple(inter.shape), pool.dtype)
+    ref = oracle.fwd_snapshots(p, oint, 2)
+    check_out(out, ref)
+    check_state(pool_to_host(inter), oint)
+    check_state(pool_to_host(d.state), p.state)
+    acc = np.array([1, 2, 3], np.int32)
+    gdr.gdr_rollback(d.state, d.slot, inter, torch.from_numpy(acc).to(DEV))
+    oracle.rollback(p, oint, acc)
+    torch.cuda.synchronize()
+    check_state(pool_to_host(d.state), p.state)
+    # dense start state, V = 2K
+    kw = dict(nk=w.nk, nv=w.nv, K=w.K, V=w.V, state_dtype=state_dtype, decay_is_log=True,
+              use_l2norm=w.use_l2norm, scale=w.scale, eps=w.eps)
+    init = pool[w.slot_idx]
+    ref_out, ref_final = oracle.fwd_dense(w.qkv, w.decay, w.beta, w.offsets, init, **kw)
+    out_d, final = gdr.gdr_fwd_dense(d.qkv, d.decay, d.beta, d.off, pool_to_dev(init), decay_is_log=True)
+    torch.cuda.synchronize()
+    check_out(out_d, ref_out)
+    check_state(pool_to_host(final), ref_final)
+
+
+@pytest.mark.parametrize("K", [16, 64, 128])
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("with_initial", [True, False])
 def test_dense_state_forward(K, state_dtype, with_initial):
     """initial_state / output_final_state ("core.ssm.ops.gdp.fused_recurrent")

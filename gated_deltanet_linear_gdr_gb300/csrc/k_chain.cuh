@@ -1,0 +1,337 @@
+// General multi-token kernel: forward, verify-ring and snapshot passes.
+//
+// A CTA owns one (row, value head, slice of VS value columns) for the whole
+// row and keeps its K x VS piece of the state in registers in float32
+// ("gated_delta_recurrence_fwd_gpu" summary: the state stays in registers for
+// the whole sequence).  Each warp owns 16 of the columns and all K rows:
+// lane kl = lane % LK holds RG consecutive row groups (8*RG rows, in the
+// row-pair form of gdr_state.cuh when RG is even), lane vl = lane / LK holds
+// C columns.  The K-reductions of a token therefore end
+// with log2(LK) xor-shuffles and the warps never wait for each other inside a
+// token.
+//
+// Per-token operands (raw q and k of the key head, v of the slice, alpha,
+// beta) are staged in shared memory TC tokens at a time; the CTA's warps then
+// normalise the staged q, k once per token (shared by all warps) and run the
+// TC tokens.  One sweep over the state per token applies the update of token
+// t and accumulates the reductions of token t+1 (the readout identity in
+// gdr_device.cuh makes both reductions act on the pre-decay state).
+#pragma once
+
+#include "gdr_state.cuh"
+
+namespace gdr {
+
+// Tokens per staged chunk TCX (8, 16 or 32, chosen by the launcher from the
+// caller's row-length bound); per-element beta (BPV) stages beta per token
+// like v and uses at most 8 tokens.
+template <typename ST, int K, int VV = K, bool BPV = false, int TCX = 16> struct ChainShape {
+    static constexpr int V = VV;                   // value head size: K or 2K
+    static constexpr int NG = K / 8;               // row groups
+    static constexpr int LK = NG >= 4 ? cmin(4, NG / 2) : NG;  // lanes along K
+    static constexpr int RG = NG / LK;             // groups per lane
+    static constexpr bool RPAIR = RG % 2 == 0;     // row-pair register form
+    static constexpr int ROWS = RG * 8;            // rows per lane
+    static constexpr int LV = 32 / LK;             // lanes along V
+    static constexpr int C = cmin(2, V / LV);      // columns per lane
+    static constexpr int WC = LV * C;              // columns per warp
+    static constexpr int W = cmin(4, V / WC);      // warps per CTA
+    static constexpr int NT = 32 * W;
+    static constexpr int VS = W * WC;              // columns per CTA
+    static constexpr int SLICES = V / VS;
+    static constexpr int KP = K + LK * 4;          // padded staged vector length
+    static constexpr int TC = BPV ? cmin(8, TCX) : TCX;  // tokens per staged chunk
+    // dynamic shared memory, in floats: q, k [2][TC][KP]; v [2][TC][VS];
+    // {alpha, beta, k^.q~, -} [2][TC][4]; per-element beta [2][TC][VS]
+    static constexpr int SM_Q = 0, SM_K = SM_Q + 2 * TC * KP, SM_V = SM_K + 2 * TC * KP;
+    static constexpr int SM_SC = SM_V + 2 * TC * VS, SM_B = SM_SC + 2 * TC * 4;
+    static constexpr int SMEM = (SM_B + (BPV ? 2 * TC * VS : 0)) * 4;  // bytes
+    static constexpr int NL = NG / (RPAIR ? 2 : 1);  // lanes per token when normalising
+    static constexpr int TPW = 32 / NL;            // tokens per warp when normalising
+    using State = LaneState<RG, C>;
+};
+
+// Shared-memory index of raw row i (natural order, padded every ROWS rows).
+template <int ROWS> __device__ __forceinline__ int pidx(int i) { return vpos<false, ROWS>(i); }
+
+template <typename ST, int K, int VV, Mode MODE, bool BPV, int TCX>
+__global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX>::NT, 4)
+    k_chain(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len) {
+    using Sh = ChainShape<ST, K, VV, BPV, TCX>;
+    constexpr int V = VV, LK = Sh::LK, ROWS = Sh::ROWS, C = Sh::C;
+    constexpr int WC = Sh::WC, W = Sh::W, NT = Sh::NT, VS = Sh::VS, SLICES = Sh::SLICES;
+    constexpr int KP = Sh::KP, TC = Sh::TC, NL = Sh::NL, TPW = Sh::TPW;
+
+    // two chunk buffers: chunk i+1 is copied in while chunk i is processed
+    extern __shared__ __align__(16) float chain_smem[];
+    float(*q_s)[TC][KP] = reinterpret_cast<float(*)[TC][KP]>(chain_smem + Sh::SM_Q);
+    float(*k_s)[TC][KP] = reinterpret_cast<float(*)[TC][KP]>(chain_smem + Sh::SM_K);
+    float(*v_s)[TC][VS] = reinterpret_cast<float(*)[TC][VS]>(chain_smem + Sh::SM_V);
+    float(*sc_s)[TC][4] = reinterpret_cast<float(*)[TC][4]>(chain_smem + Sh::SM_SC);  // decay -> alpha, beta, k^.q~
+    float(*b_s)[TC][VS] = reinterpret_cast<float(*)[TC][VS]>(chain_smem + Sh::SM_B);  // per-element beta
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int kl = lane % LK, vl = lane / LK;
+    const int slice = (int)(blockIdx.x % SLICES);
+    const long long bh = blockIdx.x / SLICES;
+    const int h = (int)(bh % p.nv);
+    const int b = (int)(bh / p.nv);
+    const bool leader = tid == 0 && slice == 0 && h == 0;
+
+    const int t0 = p.offsets[b], t1 = p.offsets[b + 1];
+    if (t0 < 0 || t1 < t0 || t1 > p.T) {
+        if (leader) flag(p.status, GDR_STATUS_BAD_OFFSETS);
+        return;
+    }
+    const int L = t1 - t0;
+    if (L == 0 && !p.dense) return;  // the dense mode still hands the start state on
+    if (max_len > 0 && L > max_len) {
+        if (leader) flag(p.status, GDR_STATUS_ROW_TOO_LONG);
+        return;
+    }
+    const int wcol = warp * WC + vl * C;           // lane's first column inside the slice
+    const int col0 = slice * VS + wcol;            // ... inside the head
+    float *obase = p.out + (long long)t0 * p.out_ss + (long long)(h * V + col0) * p.out_vs;
+    const int slot = p.dense ? b : p.slot_idx[b];
+    if (slot < 0 || slot >= p.max_slots) {
+        if (slot != -1 && leader) flag(p.status, GDR_STATUS_BAD_SLOT);
+        if (kl == 0) {
+            float z[C];
+#pragma unroll
+            for (int c = 0; c < C; ++c) z[c] = 0.0f;
+            for (int t = 0; t < L; ++t) store_f32<C>(obase + (long long)t * p.out_ss, p.out_vs, p.out_vec, z);
+        }
+        return;
+    }
+
+    // Verify: rows of at most ring_len tokens record; longer rows commit.
+    bool records = false, commit = true;
+    long long ring_row = 0;  // element index of this (ring row, key head)'s first record
+    const int hk = h / p.r, jr = h % p.r;
+    if constexpr (MODE == Mode::Verify) {
+        if (L <= rp.len) {
+            commit = false;
+            const int rs = rp.ring_slot[b];
+            if (rs < 0 || rs >= rp.rows) {
+                if (leader) flag(p.status, GDR_STATUS_BAD_RING_SLOT);
+            } else {
+                records = true;
+                ring_row = ((long long)rs * p.nk + hk) * rp.len * rp.stride;
+            }
+        }
+    }
+
+    // State piece: rows kl*ROWS .. +ROWS, columns col0 .. col0+C, read from
+    // state_in (zeros when null) and committed to state_out.
+    const long long soff = (long long)slot * p.st_slot + (long long)h * p.st_head + (long long)(kl * ROWS) * p.st_k + col0;
+    const ST *sin = p.state_in ? reinterpret_cast<const ST *>(p.state_in) + soff : nullptr;
+    typename Sh::State s;
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+        Pack<ST, C> x;
+        if (sin)
+            x.load(sin + i * p.st_k);
+        else
+            x.u.v = {};
+#pragma unroll
+        for (int c = 0; c < C; ++c) s.set(i, c, x.get(c));
+    }
+
+    const long long qoff = (long long)(hk * K) * p.qkv_cs;
+    const long long koff = (long long)(p.nk * K + hk * K) * p.qkv_cs;
+    const long long voff = (long long)(2 * p.nk * K + h * V + slice * VS) * p.qkv_cs;
+    const float *bbase = p.beta + (long long)h * p.beta_hs + (long long)(slice * VS) * p.beta_vs;  // BPV
+    bool overflow = false;
+
+    // Raw operands of tokens [cb, cb + tc) into buffer bi; one cp.async group.
+    auto stage = [&](int cb, int tc, int bi) {
+        if (p.qkv_vec) {
+            constexpr int RQ = K / 4, RVS = VS / 4, RT = 2 * RQ + RVS;
+            for (int idx = tid; idx < tc * RT; idx += NT) {
+                const int tt = idx / RT, r = idx - tt * RT;
+                const float *row = p.qkv + (long long)(t0 + cb + tt) * p.qkv_ss;
+                if (r < RQ)
+                    cp_async16(&q_s[bi][tt][pidx<ROWS>(4 * r)], row + qoff + 4 * r);
+                else if (r < 2 * RQ)
+                    cp_async16(&k_s[bi][tt][pidx<ROWS>(4 * (r - RQ))], row + koff + 4 * (r - RQ));
+                else
+                    cp_async16(&v_s[bi][tt][4 * (r - 2 * RQ)], row + voff + 4 * (r - 2 * RQ));
+            }
+            for (int tt = tid; tt < tc; tt += NT) {
+                const long long o = (long long)(t0 + cb + tt) * p.tok_ss + (long long)h * p.tok_hs;
+                cp_async4(&sc_s[bi][tt][0], p.decay + o);
+                if constexpr (!BPV) cp_async4(&sc_s[bi][tt][1], p.beta + o);
+            }
+        } else {
+            for (int idx = tid; idx < tc * K; idx += NT) {
+                const int tt = idx / K, i = idx - tt * K;
+                const float *row = p.qkv + (long long)(t0 + cb + tt) * p.qkv_ss;
+                q_s[bi][tt][pidx<ROWS>(i)] = row[qoff + (long long)i * p.qkv_cs];
+                k_s[bi][tt][pidx<ROWS>(i)] = row[koff + (long long)i * p.qkv_cs];
+            }
+            for (int idx = tid; idx < tc * VS; idx += NT) {
+                const int tt = idx / VS, j = idx - tt * VS;
+                v_s[bi][tt][j] = p.qkv[(long long)(t0 + cb + tt) * p.qkv_ss + voff + (long long)j * p.qkv_cs];
+            }
+            for (int tt = tid; tt < tc; tt += NT) {
+                const long long o = (long long)(t0 + cb + tt) * p.tok_ss + (long long)h * p.tok_hs;
+                sc_s[bi][tt][0] = p.decay[o];
+                if constexpr (!BPV) sc_s[bi][tt][1] = p.beta[o];
+            }
+        }
+        if constexpr (BPV) {
+            if (p.beta_vec) {
+                constexpr int RVS = VS / 4;
+                for (int idx = tid; idx < tc * RVS; idx += NT) {
+                    const int tt = idx / RVS, r = idx - tt * RVS;
+                    cp_async16(&b_s[bi][tt][4 * r], bbase + (long long)(t0 + cb + tt) * p.beta_ss + 4 * r);
+                }
+            } else {
+                for (int idx = tid; idx < tc * VS; idx += NT) {
+                    const int tt = idx / VS, j = idx - tt * VS;
+                    b_s[bi][tt][j] = bbase[(long long)(t0 + cb + tt) * p.beta_ss + (long long)j * p.beta_vs];
+                }
+            }
+        }
+        cp_async_commit();
+    };
+
+    const int nch = (L + TC - 1) / TC;
+    stage(0, min(TC, L), 0);
+    for (int ci = 0; ci < nch; ++ci) {
+        const int cb = ci * TC, tc = min(TC, L - cb), bi = ci & 1;
+        if (ci + 1 < nch) {
+            stage(cb + TC, min(TC, L - cb - TC), bi ^ 1);  // its buffer was released at the end of ci-1
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        float(*qb)[KP] = q_s[bi];
+        float(*kb)[KP] = k_s[bi];
+        float(*vb)[VS] = v_s[bi];
+        float(*sb)[4] = sc_s[bi];
+        // ---- normalise: NL lanes per token; warp w takes tokens w, w + W, ...
+        const bool rec_alpha = records && slice == 0, rec_k = rec_alpha && jr == 0;
+        for (int tb = 0; tb < tc; tb += W * TPW) {
+            const int tt = tb + warp + W * (lane / NL);
+            const bool act = tt < tc;
+            const int ts = act ? tt : 0;
+            const long long rec = ring_row + (long long)(cb + ts) * rp.stride;
+            norm_token<K, Sh::RPAIR, ROWS>(qb[ts], kb[ts], &sb[ts][2], lane % NL, act, p,
+                                           rec_k ? rp.ring : nullptr, rp.bf16, rec);
+            if (act && lane % NL == 0) {
+                const float alpha = gdr_alpha(sb[ts][0], p.decay_is_log);
+                sb[ts][0] = alpha;
+                if (rec_alpha) ring_put1(rp.ring, rp.bf16, rec + rp.alpha_off + jr, alpha);
+            }
+        }
+        __syncthreads();
+
+        // ---- reductions of the chunk's first token
+        const int rb = pidx<ROWS>(kl * ROWS);  // start of this lane's rows in the staged vectors
+        float a[C], bq[C];
+        s.partials(&kb[0][rb], &qb[0][rb], a, bq);
+
+        // ---- the chunk's tokens
+        for (int tt = 0; tt < tc; ++tt) {
+            const float alpha = sb[tt][0], beta = sb[tt][1], kq = sb[tt][2];
+            float u[C], o[C];
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                const float A = tree_lanes<LK>(a[c]);
+                const float B = tree_lanes<LK>(bq[c]);
+                const float bj = BPV ? b_s[bi][tt][wcol + c] : beta;
+                u[c] = gdr_u(bj, alpha, A, vb[tt][wcol + c]);
+                o[c] = gdr_o(alpha, B, kq, u[c]);
+            }
+            const int step = cb + tt;  // token index inside the row
+            if (kl == 0) store_f32<C>(obase + (long long)step * p.out_ss, p.out_vs, p.out_vec, o);
+            if constexpr (MODE == Mode::Verify) {
+                if (records && kl == 0) {
+                    const long long rec = ring_row + (long long)step * rp.stride + rp.u_off + jr * V + col0;
+                    if constexpr (C % 2 == 0) {
+#pragma unroll
+                        for (int c = 0; c < C; c += 2) ring_put2(rp.ring, rp.bf16, rec + c, u[c], u[c + 1]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < C; ++c) ring_put1(rp.ring, rp.bf16, rec + c, u[c]);
+                    }
+                }
+            }
+            // One sweep: S <- k^_t u^T + alpha S, and token t+1's partials on the new S
+            // (the chunk's last token sweeps against its own vectors; those partials
+            // are discarded and recomputed once the next chunk is normalised).
+            const int tn = tt + 1 < tc ? tt + 1 : tt;
+            s.advance_partials(&kb[tt][rb], &kb[tn][rb], &qb[tn][rb], u, alpha, a, bq);
+            if constexpr (MODE == Mode::Snap) {
+                if ((step + 1) % sp.spt == 0) {
+                    const int i = (step + 1) / sp.spt - 1;
+                    if (i < sp.n_inter) {
+                        ST *it = reinterpret_cast<ST *>(sp.inter) + (long long)slot * sp.s_slot +
+                                 (long long)i * sp.s_tok + (long long)h * sp.s_head +
+                                 (long long)(kl * ROWS) * V + col0;
+#pragma unroll
+                        for (int r = 0; r < ROWS; ++r) {
+                            Pack<ST, C> x;
+#pragma unroll
+                            for (int c = 0; c < C; ++c) x.set(c, s.get(r, c));
+                            x.store(it + r * V);
+                        }
+                    } else {
+                        overflow = true;
+                    }
+                }
+            }
+        }
+        __syncthreads();  // every warp is done with buffer bi before chunk ci+2 is copied into it
+    }
+    if constexpr (MODE == Mode::Snap) {
+        if (overflow && leader) flag(p.status, GDR_STATUS_SNAPSHOT_OVERFLOW);
+    }
+    (void)records;
+    if (commit && p.state_out) {
+        ST *sout = reinterpret_cast<ST *>(p.state_out) + soff;
+#pragma unroll
+        for (int i = 0; i < ROWS; ++i) {
+            Pack<ST, C> x;
+#pragma unroll
+            for (int c = 0; c < C; ++c) x.set(c, s.get(i, c));
+            x.store(sout + i * p.st_k);
+        }
+    }
+}
+
+// Chunk tokens of the forward pass over long or unbounded rows.
+constexpr int kChainLongTC = 32;
+
+// The launchers of each pass (one translation unit each, so they compile in
+// parallel); blocks = batch * nv * SLICES.
+cudaError_t launch_chain_fwd(const StepParams &p, int K, int V, bool bf16, long long max_len, cudaStream_t st);
+cudaError_t launch_chain_verify(const StepParams &p, int K, bool bf16, const RingParams &rp, long long max_len,
+                                cudaStream_t st);
+cudaError_t launch_chain_snap(const StepParams &p, int K, int V, bool bf16, const SnapParams &sp, long long max_len,
+                              cudaStream_t st);
+
+// Launches one instantiation with its dynamic shared memory (opted in once per
+// device above 48 KiB).
+template <typename ST, int K, int V, Mode MODE, bool BPV, int TCX>
+inline cudaError_t launch_chain_k(const StepParams &p, const RingParams &rp, const SnapParams &sp,
+                                  long long max_len, long long blocks, cudaStream_t st) {
+    using Sh = ChainShape<ST, K, V, BPV, TCX>;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(k_chain<ST, K, V, MODE, BPV, TCX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Sh::SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = 1;
+    }
+    k_chain<ST, K, V, MODE, BPV, TCX><<<(unsigned)blocks, Sh::NT, Sh::SMEM, st>>>(p, rp, sp, max_len);
+    return cudaGetLastError();
+}
+
+}  // namespace gdr

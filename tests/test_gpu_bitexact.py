@@ -60,6 +60,60 @@ def test_verify_output_equals_forward_and_pool_untouched(state_dtype):
             assert (host[s] == pool[s]).all(), "verify must leave the pool alone"
 
 
+def test_prepared_calls_replay_from_a_cuda_graph():
+    """The entry points never synchronise or read device memory on the host, so
+    a decode step and a verify + fold window captured into a CUDA graph replay
+    with the same bits as direct calls."""
+    w = W.decode(batch=64, max_slots=128)
+    pool = w.state_pool()
+    direct = Dev(w, pool)
+    out_direct = direct.fwd(max_row_len=1).clone()
+    captured = Dev(w, pool)
+    out = torch.empty_like(out_direct)
+    call = gdr.prepare_fwd(captured.qkv, captured.decay, captured.beta, captured.state, captured.slot,
+                           captured.off, out, max_row_len=1)
+    call()  # warm-up outside the graph (loads the library, sets kernel attributes)
+    torch.cuda.synchronize()
+    captured.state.copy_(pool_to_dev(pool))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    g.replay()
+    torch.cuda.synchronize()
+    assert (out.view(torch.int32) == out_direct.view(torch.int32)).all()
+    assert (pool_to_host(captured.state) == pool_to_host(direct.state)).all()
+
+    wv = W.verify_fold(batch=16, max_slots=32, ring_rows=32)
+    pv = wv.state_pool()
+    res = []
+    for use_graph in (False, True):
+        d = Dev(wv, pv)
+        ring = ring_for(wv, wv.ring_len, wv.ring_rows)
+        rsi = torch.from_numpy(wv.ring_slot_idx).to(DEV)
+        o = torch.empty((wv.total_tokens, wv.nv * wv.V), device=DEV)
+        v = gdr.prepare_verify_ring(d.qkv, d.decay, d.beta, d.state, d.slot, d.off, ring, rsi, o,
+                                    max_row_len=12)
+        f = gdr.prepare_fold(d.state, d.slot, ring, rsi, torch.from_numpy(wv.counts).to(DEV))
+        if use_graph:
+            v()
+            f()
+            torch.cuda.synchronize()
+            d.state.copy_(pool_to_dev(pv))
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2):
+                v()
+                f()
+            g2.replay()
+        else:
+            v()
+            f()
+        torch.cuda.synchronize()
+        res.append((o.cpu().numpy(), pool_to_host(d.state)))
+    assert (res[0][0].view(np.uint32) == res[1][0].view(np.uint32)).all()
+    assert (res[0][1] == res[1][1]).all()
+    assert gdr.gdr_get_status(clear=True) == 0
+
+
 @pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
 def test_value_head_twice_key_head_equals_two_halves(state_dtype):
     """The value columns never mix: a V = 2K pass gives, bit for bit, the two

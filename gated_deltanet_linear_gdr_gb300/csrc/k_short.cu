@@ -313,7 +313,9 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
             }
             optr += p.out_ss;
             uidx += rp.stride;
-            s.advance(tk + base, u, alpha);  // S <- k^ u^T + alpha S
+            // S <- k^ u^T + alpha S; a verify row that does not commit never
+            // reads the state after its last token
+            if (commit || cb + tt + 1 < L) s.advance(tk + base, u, alpha);
         }
     }
     if (commit) short_put_tile<ST, K>(stage, r0, col, s);

@@ -54,9 +54,40 @@ template <typename ST, int K, int VV = K, bool BPV = false, int TCX = 16> struct
 // Shared-memory index of raw row i (natural order, padded every ROWS rows).
 template <int ROWS> __device__ __forceinline__ int pidx(int i) { return vpos<false, ROWS>(i); }
 
+// Block -> unit for a few long rows of unequal length (every thread of the
+// CTA calls it; needs blockDim.x >= batch).  A CTA owns its row for the whole
+// row, so the time of the call is set by the SM whose resident CTAs hold the
+// most tokens.  Units are taken in order of decreasing row length (ties by
+// row index) and dealt to the blocks as a snake: pass j covers blocks
+// jP .. jP+P-1 (P = SMs), forward on even passes and backward on odd ones,
+// so when the first wave is spread over the SMs in a fixed order the long
+// and short rows pair up on each SM.  Any placement still gets every unit
+// exactly once.
+__device__ __forceinline__ long long chain_balanced_unit(const StepParams &p, int slices, int P) {
+    __shared__ int row_of_rank;
+    const long long per_row = (long long)p.nv * slices;
+    const long long n = (long long)p.batch * per_row;
+    const long long i = blockIdx.x, pass = i / P, pos = i - pass * P;
+    const long long m = n - pass * P < P ? n - pass * P : P;  // blocks in this pass
+    const long long k = pass * P + ((pass & 1) ? m - 1 - pos : pos);
+    const int rank = (int)(k / per_row);
+    const int r = threadIdx.x;
+    if (r < p.batch) {
+        const int Lr = p.offsets[r + 1] - p.offsets[r];
+        int rk = 0;
+        for (int j = 0; j < p.batch; ++j) {
+            const int Lj = p.offsets[j + 1] - p.offsets[j];
+            rk += (Lj > Lr || (Lj == Lr && j < r)) ? 1 : 0;
+        }
+        if (rk == rank) row_of_rank = r;
+    }
+    __syncthreads();
+    return (long long)row_of_rank * per_row + (k - (long long)rank * per_row);
+}
+
 template <typename ST, int K, int VV, Mode MODE, bool BPV, int TCX>
 __global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX>::NT, 4)
-    k_chain(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len) {
+    k_chain(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len, const int order_p) {
     using Sh = ChainShape<ST, K, VV, BPV, TCX>;
     constexpr int V = VV, LK = Sh::LK, ROWS = Sh::ROWS, C = Sh::C;
     constexpr int WC = Sh::WC, W = Sh::W, NT = Sh::NT, VS = Sh::VS, SLICES = Sh::SLICES;
@@ -72,8 +103,9 @@ __global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX>::NT, 4)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kl = lane % LK, vl = lane / LK;
-    const int slice = (int)(blockIdx.x % SLICES);
-    const long long bh = blockIdx.x / SLICES;
+    const long long unit = order_p > 0 ? chain_balanced_unit(p, SLICES, order_p) : (long long)blockIdx.x;
+    const int slice = (int)(unit % SLICES);
+    const long long bh = unit / SLICES;
     const int h = (int)(bh % p.nv);
     const int b = (int)(bh / p.nv);
     const bool leader = tid == 0 && slice == 0 && h == 0;
@@ -305,6 +337,9 @@ __global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX>::NT, 4)
 // Chunk tokens of the forward pass over long or unbounded rows.
 constexpr int kChainLongTC = 32;
 
+// Batches of at most this many rows are dealt out longest row first.
+constexpr int kChainOrderRows = 32;
+
 // The launchers of each pass (one translation unit each, so they compile in
 // parallel); blocks = batch * nv * SLICES.
 cudaError_t launch_chain_fwd(const StepParams &p, int K, int V, bool bf16, long long max_len, cudaStream_t st);
@@ -319,7 +354,7 @@ template <typename ST, int K, int V, Mode MODE, bool BPV, int TCX>
 inline cudaError_t launch_chain_k(const StepParams &p, const RingParams &rp, const SnapParams &sp,
                                   long long max_len, long long blocks, cudaStream_t st) {
     using Sh = ChainShape<ST, K, V, BPV, TCX>;
-    static int configured[64] = {0};
+    static int configured[64] = {0}, sms[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -328,9 +363,13 @@ inline cudaError_t launch_chain_k(const StepParams &p, const RingParams &rp, con
         e = cudaFuncSetAttribute(k_chain<ST, K, V, MODE, BPV, TCX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Sh::SMEM);
         if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
-    k_chain<ST, K, V, MODE, BPV, TCX><<<(unsigned)blocks, Sh::NT, Sh::SMEM, st>>>(p, rp, sp, max_len);
+    // a few rows: deal them out longest first (chain_balanced_unit)
+    const int order_p = (p.batch <= Sh::NT && p.batch <= kChainOrderRows && blocks > sms[dev]) ? sms[dev] : 0;
+    k_chain<ST, K, V, MODE, BPV, TCX><<<(unsigned)blocks, Sh::NT, Sh::SMEM, st>>>(p, rp, sp, max_len, order_p);
     return cudaGetLastError();
 }
 

@@ -6,8 +6,9 @@ decode step: batch 256 rows x 1 token (8 padding rows), nk=16, nv=32,
 K=V=128, float32 per-token inputs, bf16 state pool [512, 32, 128, 128] read
 and written in place.  `value` is head-tokens/s (live tokens x nv per step /
 step time) with inputs resident in HBM; `e2e` is the same metric through the
-public Python API with the step's inputs copied from pinned host memory and
-the output copied back inside the timed region.  The L2 cache is flushed
+C-ABI host-buffer entry point gdr_fwd_host (binding: HostForward): the step's
+inputs are copied from pinned host memory and the output copied back inside
+the timed region, row groups pipelined against the compute.  The L2 cache is flushed
 (a read-only sweep of a 2x-L2 buffer) before every timed step.
 
 Secondary workloads (ragged prefill, verify + fold, Gated Delta Product
@@ -216,18 +217,16 @@ class DecodeStep:
         self.call = gdr.prepare_fwd(d["qkv"], d["decay"], d["beta"], self.state, d["slot"],
                                     d["off"], self.out, max_row_len=1)
         self.stream = torch.cuda.current_stream(dev).cuda_stream
+        # end to end: the host-buffer entry point (tokens copied in, row groups
+        # pipelined against the compute, output copied back, in one C-ABI call)
+        self.host_fwd = gdr.HostForward(self.state, w.nk, w.batch, w.total_tokens, max_row_len=1)
 
     def run(self):
         self.call(self.stream)
 
     def run_e2e(self):
-        import gated_deltanet_linear_gdr_gb300 as gdr
-        d, h = self.d, self.h
-        for k in d:
-            d[k].copy_(h[k], non_blocking=True)
-        gdr.gdr_fwd(d["qkv"], d["decay"], d["beta"], self.state, d["slot"], d["off"],
-                    out=self.out, max_row_len=1)
-        self.h_out.copy_(self.out, non_blocking=True)
+        h = self.h
+        self.host_fwd(h["qkv"], h["decay"], h["beta"], h["slot"], h["off"], self.h_out, self.stream)
 
 
 def time_steps(fn, steps, flush, stream):

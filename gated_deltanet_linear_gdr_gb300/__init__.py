@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     GDR_BF16,
     GDR_F32,
     GdrError,
+    HostForward,
     gdr_fold,
     gdr_fwd,
     gdr_fwd_dense,

@@ -33,6 +33,14 @@ class GdrError(RuntimeError):
         self.code = code
 
 
+class gdr_host_io(ctypes.Structure):
+    """Mirror of struct gdr_host_io in include/gdr.h (host pointers)."""
+    _fields_ = [
+        ("qkv", ctypes.c_void_p), ("decay", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+        ("slot_idx", ctypes.c_void_p), ("offsets", ctypes.c_void_p), ("out", ctypes.c_void_p),
+    ]
+
+
 class gdr_step_args(ctypes.Structure):
     """Mirror of struct gdr_step_args in include/gdr.h (same order and types)."""
     _fields_ = [
@@ -80,6 +88,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                 "gdr_output_shape": ([i64, i32, i32, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
                 "gdr_ring_record_elements": ([i32, i32, i32], ctypes.c_int),
                 "gdr_fwd": ([A, vp], ctypes.c_int),
+                "gdr_fwd_host": ([A, ctypes.POINTER(gdr_host_io), i32, vp, vp, vp], ctypes.c_int),
                 "gdr_fwd_dense": ([A, vp, vp, vp], ctypes.c_int),
                 "gdr_verify_ring": ([A, vp, i32, i64, i32, i64, vp, vp], ctypes.c_int),
                 "gdr_fold": ([A, vp, i32, i64, i32, i64, vp, vp, vp], ctypes.c_int),
@@ -219,6 +228,65 @@ def gdr_fwd(qkv, decay, beta, state, slot_idx, offsets, out=None, *, decay_is_lo
                   max_row_len=max_row_len)
     _check(load_library().gdr_fwd(ctypes.byref(a), _stream(qkv.device)))
     return out
+
+
+def _host(t: torch.Tensor, name: str, dtype):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) torch.Tensor")
+    if t.dtype != dtype or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous {dtype} tensor")
+    return t
+
+
+class HostForward:
+    """gdr_fwd_host for host-resident tokens: the forward pass
+    ("gated_delta_recurrence_fwd_gpu") with the tokens copied in and the
+    output copied back inside one C-ABI call, row groups pipelined over three
+    streams (copies in, compute, copies out).
+
+    Owns the device staging buffers for batches of up to `batch` rows and
+    `total_tokens` tokens and the two side streams; the pool stays the
+    caller's device tensor.  Host tensors should be pinned
+    (tensor.pin_memory()) for the copies to overlap the compute."""
+
+    def __init__(self, state, nk: int, batch: int, total_tokens: int, *, decay_is_log=False,
+                 use_qk_l2norm=True, scale=0.0, eps=1e-6, max_row_len=0, chunks=0):
+        _dev(state, "state", (torch.bfloat16, torch.float32))
+        dev = state.device
+        nv, K, V = state.shape[1:]
+        f32, i32 = torch.float32, torch.int32
+        self.state = state
+        self.qkv = torch.empty((total_tokens, 2 * nk * K + nv * V), dtype=f32, device=dev)
+        self.decay = torch.empty((total_tokens, nv), dtype=f32, device=dev)
+        self.beta = torch.empty((total_tokens, nv), dtype=f32, device=dev)
+        self.out = torch.empty((total_tokens, nv * V), dtype=f32, device=dev)
+        self.slot_idx = torch.empty((batch,), dtype=i32, device=dev)
+        self.offsets = torch.empty((batch + 1,), dtype=i32, device=dev)
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.chunks = int(chunks)
+        self.args = make_args(self.qkv, self.decay, self.beta, state, self.slot_idx, self.offsets, self.out,
+                              nk=nk, decay_is_log=decay_is_log, use_qk_l2norm=use_qk_l2norm, scale=scale,
+                              eps=eps, max_row_len=max_row_len)
+        self.device = dev
+
+    def __call__(self, qkv, decay, beta, slot_idx, offsets, out, stream: Optional[int] = None):
+        """Runs the pass on host tensors; `out` (host, [T, nv*V]) holds the
+        result once `stream` (default: the current stream) has passed the call."""
+        for t, n, d in ((qkv, "qkv", torch.float32), (decay, "decay", torch.float32),
+                        (beta, "beta", torch.float32), (slot_idx, "slot_idx", torch.int32),
+                        (offsets, "offsets", torch.int32), (out, "out", torch.float32)):
+            _host(t, n, d)
+        if tuple(qkv.shape) != tuple(self.qkv.shape) or tuple(out.shape) != tuple(self.out.shape):
+            raise ValueError("qkv / out shapes differ from the staging buffers")
+        if slot_idx.shape[0] != self.slot_idx.shape[0] or offsets.shape[0] != self.offsets.shape[0]:
+            raise ValueError("slot_idx / offsets lengths differ from the staging buffers")
+        io = gdr_host_io(qkv.data_ptr(), decay.data_ptr(), beta.data_ptr(), slot_idx.data_ptr(),
+                         offsets.data_ptr(), out.data_ptr())
+        s = _stream(self.device) if stream is None else stream
+        _check(load_library().gdr_fwd_host(ctypes.byref(self.args), ctypes.byref(io), self.chunks, s,
+                                           self.h2d.cuda_stream, self.d2h.cuda_stream))
+        return out
 
 
 def gdr_fwd_dense(qkv, decay, beta, offsets, initial_state=None, output_final_state=True, out=None, *,

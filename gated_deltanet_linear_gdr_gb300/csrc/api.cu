@@ -174,6 +174,53 @@ cudaError_t launch_rows(const gdr::StepParams &p, const gdr_step_args *a, gdr::M
     return gdr::launch_chain(p, a->K, a->V, bf16, mode, rp, sp, a->max_row_len, s);
 }
 
+// The forward dispatch shared by gdr_fwd and gdr_fwd_host (arguments checked).
+cudaError_t launch_fwd(const gdr_step_args *a, unsigned *status, cudaStream_t s) {
+    const gdr::StepParams p = lower(a, status);
+    if (a->max_row_len == 1 && !p.bpv && a->V == a->K) return gdr::launch_decode(p, a->K, a->state_dtype == GDR_BF16, s);
+    return launch_rows(p, a, gdr::Mode::Fwd, gdr::RingParams{}, gdr::SnapParams{}, s);
+}
+
+// Row groups of gdr_fwd_host: the default count and the limit.
+constexpr int kHostChunksAuto = 4;
+constexpr int kHostMaxChunks = 16;
+
+// Events that order gdr_fwd_host's copies and kernels across streams: one set
+// per host thread and device, created on first use and kept until exit.
+struct HostEvents {
+    cudaEvent_t start, end, in[kHostMaxChunks], done[kHostMaxChunks];
+};
+
+int host_events(HostEvents **out) {
+    static thread_local HostEvents *sets[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(GDR_ERR_CUDA, "device ordinal %d out of range", dev);
+    if (!sets[dev]) {
+        HostEvents *h = new HostEvents;
+        cudaEvent_t *all[2 + 2 * kHostMaxChunks];
+        int n = 0;
+        all[n++] = &h->start;
+        all[n++] = &h->end;
+        for (int c = 0; c < kHostMaxChunks; ++c) {
+            all[n++] = &h->in[c];
+            all[n++] = &h->done[c];
+        }
+        for (int i = 0; i < n; ++i) {
+            e = cudaEventCreateWithFlags(all[i], cudaEventDisableTiming);
+            if (e != cudaSuccess) {
+                for (int j = 0; j < i; ++j) cudaEventDestroy(*all[j]);
+                delete h;
+                return fail(GDR_ERR_CUDA, "cudaEventCreateWithFlags: %s", cudaGetErrorString(e));
+            }
+        }
+        sets[dev] = h;
+    }
+    *out = sets[dev];
+    return GDR_OK;
+}
+
 int launched(cudaError_t e, const char *fn) {
     if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
     return ok();
@@ -242,11 +289,101 @@ int gdr_fwd(const gdr_step_args *a, void *stream) {
     if (a->batch == 0) return ok();
     unsigned *st = nullptr;
     if ((rc = status_ptr(&st))) return rc;
-    const gdr::StepParams p = lower(a, st);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (a->max_row_len == 1 && !p.bpv && a->V == a->K)
-        return launched(gdr::launch_decode(p, a->K, a->state_dtype == GDR_BF16, s), "gdr_fwd");
-    return launched(launch_rows(p, a, gdr::Mode::Fwd, gdr::RingParams{}, gdr::SnapParams{}, s), "gdr_fwd");
+    return launched(launch_fwd(a, st, static_cast<cudaStream_t>(stream)), "gdr_fwd");
+}
+
+int gdr_fwd_host(const gdr_step_args *a, const gdr_host_io *h, int32_t chunks, void *stream, void *h2d_stream,
+                 void *d2h_stream) {
+    const char *fn = "gdr_fwd_host";
+    int rc = check_step(a, fn);
+    if (rc) return rc;
+    if (!h) return fail(GDR_ERR_INVALID_ARG, "%s: host is NULL", fn);
+    if (a->batch == 0) return ok();
+    if (!h->qkv || !h->decay || !h->beta || !h->slot_idx || !h->offsets || !h->out)
+        return fail(GDR_ERR_INVALID_ARG, "%s: a host buffer is NULL", fn);
+    const int64_t conv = 2ll * a->nk * a->K + (int64_t)a->nv * a->V, ow = (int64_t)a->nv * a->V;
+    if (a->beta_vdim_stride > 0)
+        return fail(GDR_ERR_UNSUPPORTED, "%s: beta must be [total_tokens, nv] (beta_vdim_stride 0)", fn);
+    if (a->total_tokens > 0 &&
+        (a->qkv_chan_stride != 1 || a->qkv_seq_stride != conv || a->tok_head_stride != 1 ||
+         a->tok_seq_stride != a->nv || a->out_vdim_stride != 1 || a->out_seq_stride != ow))
+        return fail(GDR_ERR_UNSUPPORTED, "%s: device token buffers must be dense", fn);
+    const int32_t *off = h->offsets;
+    if (off[0] < 0 || off[a->batch] > a->total_tokens)
+        return fail(GDR_ERR_INVALID_ARG, "%s: offsets outside [0, total_tokens]", fn);
+    for (int b = 0; b < a->batch; ++b)
+        if (off[b + 1] < off[b]) return fail(GDR_ERR_INVALID_ARG, "%s: offsets not monotone at row %d", fn, b);
+    unsigned *st = nullptr;
+    if ((rc = status_ptr(&st))) return rc;
+    HostEvents *ev = nullptr;
+    if ((rc = host_events(&ev))) return rc;
+
+    // groups of consecutive rows with about equal token counts
+    int nch = chunks > 0 ? chunks : kHostChunksAuto;
+    if (nch > kHostMaxChunks) nch = kHostMaxChunks;
+    if (nch > a->batch) nch = a->batch;
+    int bound[kHostMaxChunks + 1];
+    bound[0] = 0;
+    const int64_t T0 = off[0], span = (int64_t)off[a->batch] - off[0];
+    for (int c = 1; c < nch; ++c) {
+        const int64_t target = T0 + span * c / nch;
+        int r = bound[c - 1] + 1;  // every group keeps at least one row
+        while (r < a->batch - (nch - c) && off[r] < target) ++r;
+        bound[c] = r;
+    }
+    bound[nch] = a->batch;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaStream_t hs = h2d_stream ? static_cast<cudaStream_t>(h2d_stream) : cs;
+    cudaStream_t ds = d2h_stream ? static_cast<cudaStream_t>(d2h_stream) : cs;
+    cudaError_t e = cudaSuccess;
+    auto cuda = [&](cudaError_t r) {
+        if (e == cudaSuccess) e = r;
+        return e == cudaSuccess;
+    };
+    auto order = [&](cudaStream_t from, cudaStream_t to, cudaEvent_t evt) {
+        if (from == to) return true;
+        return cuda(cudaEventRecord(evt, from)) && cuda(cudaStreamWaitEvent(to, evt, 0));
+    };
+    // the device buffers may still be in use by work queued earlier on `stream`
+    if (!order(cs, hs, ev->start)) return fail(GDR_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    const size_t f4 = sizeof(float), i4 = sizeof(int32_t);
+    // the small arrays (slots, offsets, decay, beta) go in whole with the first
+    // group, since every copy has a fixed cost; qkv and out travel per group
+    const int64_t T_lo = off[0], T_hi = off[a->batch];
+    bool good = cuda(cudaMemcpyAsync(const_cast<int32_t *>(a->slot_idx), h->slot_idx, (size_t)a->batch * i4,
+                                     cudaMemcpyHostToDevice, hs)) &&
+                cuda(cudaMemcpyAsync(const_cast<int32_t *>(a->offsets), h->offsets, (size_t)(a->batch + 1) * i4,
+                                     cudaMemcpyHostToDevice, hs));
+    if (good && T_hi > T_lo)
+        good = cuda(cudaMemcpyAsync(const_cast<float *>(a->decay) + T_lo * a->nv, h->decay + T_lo * a->nv,
+                                    (size_t)((T_hi - T_lo) * a->nv) * f4, cudaMemcpyHostToDevice, hs)) &&
+               cuda(cudaMemcpyAsync(const_cast<float *>(a->beta) + T_lo * a->nv, h->beta + T_lo * a->nv,
+                                    (size_t)((T_hi - T_lo) * a->nv) * f4, cudaMemcpyHostToDevice, hs));
+    if (!good) return fail(GDR_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    for (int c = 0; c < nch; ++c) {
+        const int r0 = bound[c], r1 = bound[c + 1];
+        const int64_t t0 = off[r0], t1 = off[r1];
+        const int64_t nt = t1 - t0;
+        if (nt > 0)
+            good = cuda(cudaMemcpyAsync(const_cast<float *>(a->qkv) + t0 * conv, h->qkv + t0 * conv,
+                                        (size_t)(nt * conv) * f4, cudaMemcpyHostToDevice, hs));
+        good = good && order(hs, cs, ev->in[c]);
+        if (good) {
+            gdr_step_args g = *a;
+            g.batch = r1 - r0;
+            g.slot_idx = a->slot_idx + r0;
+            g.offsets = a->offsets + r0;
+            good = cuda(launch_fwd(&g, st, cs)) && order(cs, ds, ev->done[c]);
+        }
+        if (good && nt > 0)
+            good = cuda(cudaMemcpyAsync(h->out + t0 * ow, a->out + t0 * ow, (size_t)(nt * ow) * f4,
+                                        cudaMemcpyDeviceToHost, ds));
+        if (!good) return fail(GDR_ERR_CUDA, "%s: group %d: %s", fn, c, cudaGetErrorString(e));
+    }
+    // `stream` passes the call only once every copy back has landed
+    if (!order(ds, cs, ev->end)) return fail(GDR_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    return ok();
 }
 
 int gdr_fwd_dense(const gdr_step_args *a, const void *initial_state, void *final_state, void *stream) {

@@ -20,8 +20,9 @@
  * Parameters of fused_recurrent_gated_delta_rule_update.
  *
  * Conventions shared by every entry point
- *   - Every buffer pointer is a DEVICE pointer owned by the caller; the library
- *     allocates and frees nothing and keeps no pointer after a call returns.
+ *   - Every buffer pointer is a DEVICE pointer owned by the caller (except the
+ *     host buffers of gdr_host_io); the library allocates and frees nothing and
+ *     keeps no pointer after a call returns.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream).  They never synchronise and never read device memory on the host;
  *     only gdr_get_status() synchronises.
@@ -168,6 +169,44 @@ int gdr_ring_record_elements(int32_t K, int32_t V, int32_t ratio);
  * back to its slot (bf16 pools are rounded to nearest-even once, at the row
  * end).  Rows of length 0 leave their slot untouched. */
 int gdr_fwd(const gdr_step_args *args, void *stream);
+
+/*
+ * Token inputs and output in HOST memory, for gdr_fwd_host.  Dense row-major
+ * layouts with the shapes of gdr_step_args: qkv [total_tokens, 2*nk*K + nv*V],
+ * decay and beta [total_tokens, nv], slot_idx [batch], offsets [batch+1],
+ * out [total_tokens, nv*V].  Page-locked memory lets the copies run
+ * asynchronously and overlap the compute; other host memory also works, with
+ * copies that the CUDA runtime may serialise.
+ */
+typedef struct gdr_host_io {
+    const float *qkv;
+    const float *decay;
+    const float *beta;
+    const int32_t *slot_idx;
+    const int32_t *offsets;
+    float *out;
+} gdr_host_io;
+
+/* Forward pass over host-resident tokens ("gated_delta_recurrence_fwd_gpu",
+ * the same computation as gdr_fwd, bit for bit).  `args` names the device
+ * buffers the tokens are copied into -- qkv, decay, beta, slot_idx, offsets
+ * and out, dense with the shapes above (qkv_seq_stride = 2*nk*K + nv*V,
+ * tok_seq_stride = nv, out_seq_stride = nv*V, unit inner strides, head-wise
+ * beta) -- and the device pool.  The rows are split into `chunks` groups of
+ * consecutive rows with about equal token counts (chunks <= 0: the library
+ * picks; at most 16 and at most batch).  Each group's tokens are copied in on
+ * h2d_stream, computed on `stream` and its output copied back on d2h_stream,
+ * so one group's copies overlap its neighbours' compute (a NULL side stream
+ * puts that direction on `stream`, without overlap).  Asynchronous on
+ * `stream`: work already queued there precedes the copies, and once `stream`
+ * has passed the call host->out holds every row's output and the pool the new
+ * states; until then the device buffers and host->out must not be touched.
+ * host->offsets is read on the host during the call (it must be monotone,
+ * within [0, total_tokens]).  On its first call on a device a host thread
+ * creates a few CUDA events that it keeps until exit; no memory is allocated.
+ */
+int gdr_fwd_host(const gdr_step_args *args, const gdr_host_io *host, int32_t chunks, void *stream,
+                 void *h2d_stream, void *d2h_stream);
 
 /* Forward pass with a dense start and end state ("core.ssm.ops.gdp.fused_recurrent",
  * initial_state [N, HV, K, V] or None for zeros, output_final_state): as gdr_fwd,

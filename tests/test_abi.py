@@ -239,3 +239,48 @@ def test_status_null_pointer(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="no CPU or Python fallback"):
         B.load_library(str(tmp_path / "libgdr.so"))
+
+
+def test_host_io_layout_matches_header(tmp_path):
+    fields = [f[0] for f in B.gdr_host_io._fields_]
+    prog = tmp_path / "hostio.c"
+    prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gdr.h"\nint main(void) {\n'
+                    '  printf("size %zu\\n", sizeof(gdr_host_io));\n' +
+                    "".join(f'  printf("{f} %zu\\n", offsetof(gdr_host_io, {f}));\n' for f in fields) +
+                    "  return 0;\n}\n")
+    exe = tmp_path / "hostio"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                        check=True).stdout.splitlines())
+    assert int(got["size"]) == ctypes.sizeof(B.gdr_host_io)
+    for f in fields:
+        assert int(got[f]) == getattr(B.gdr_host_io, f).offset, f
+
+
+def test_fwd_host_rejects_bad_arguments(lib):
+    """Host-side checks of gdr_fwd_host, all before any CUDA call."""
+    fake = 0x7f0000000000  # device pointers are never dereferenced on these paths
+    off = (ctypes.c_int32 * 3)(0, 5, 8)
+    io = B.gdr_host_io(fake, fake, fake, fake, ctypes.addressof(off), fake)
+    call = lambda a, h: lib.gdr_fwd_host(ctypes.byref(a), h, 0, None, None, None)
+    assert call(_valid_args(), None) == B.GDR_ERR_INVALID_ARG
+    a = _valid_args()
+    a.nk = 3  # the shared checks run first
+    assert call(a, ctypes.byref(io)) == B.GDR_ERR_INVALID_ARG
+    missing = B.gdr_host_io(fake, None, fake, fake, ctypes.addressof(off), fake)
+    assert call(_valid_args(), ctypes.byref(missing)) == B.GDR_ERR_INVALID_ARG
+    for name, value in [("qkv_seq_stride", 132), ("tok_seq_stride", 8), ("out_seq_stride", 68),
+                        ("qkv_chan_stride", 2)]:
+        a = _valid_args()
+        setattr(a, name, value)
+        assert call(a, ctypes.byref(io)) == B.GDR_ERR_UNSUPPORTED, name
+    a = _valid_args()
+    a.beta_seq_stride, a.beta_head_stride, a.beta_vdim_stride = 64, 16, 1
+    assert call(a, ctypes.byref(io)) == B.GDR_ERR_UNSUPPORTED
+    for bad in [(0, 6, 5), (0, 5, 9), (-1, 5, 8)]:
+        o = (ctypes.c_int32 * 3)(*bad)
+        h = B.gdr_host_io(fake, fake, fake, fake, ctypes.addressof(o), fake)
+        assert call(_valid_args(), ctypes.byref(h)) == B.GDR_ERR_INVALID_ARG, bad
+    a = _valid_args()
+    a.batch = 0
+    assert call(a, ctypes.byref(io)) == B.GDR_OK

@@ -497,3 +497,31 @@ def test_sliced_fold_equals_simple_fold(state_dtype, K, ring_dtype):
         outs.append(pool_to_host(st))
     assert (outs[0] == outs[1]).all()
     assert gdr.gdr_get_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("case", ["decode", "ragged"])
+@pytest.mark.parametrize("chunks", [1, 3, 0])
+def test_host_buffer_forward_equals_device_forward(case, chunks):
+    """gdr_fwd_host (tokens copied in, row groups pipelined over three streams,
+    output copied back inside one C-ABI call) gives gdr_fwd's bits: outputs,
+    padding zeros and the pool."""
+    if case == "decode":
+        w = W.decode(batch=40, max_slots=64, n_pad=3)
+        mrl = 1
+    else:
+        w = W.random_case(91, [7, 1, 0, 12, 3, 5, 9], nk=2, nv=4, K=64, max_slots=12,
+                          state_dtype="bf16", n_pad=1)
+        mrl = 0
+    pool = w.state_pool()
+    out_ref, pool_ref = _run_fwd(w, pool, max_row_len=mrl)
+    state = pool_to_dev(pool)
+    hf = gdr.HostForward(state, w.nk, w.batch, w.total_tokens, decay_is_log=w.decay_is_log,
+                         use_qk_l2norm=w.use_l2norm, scale=w.scale, eps=w.eps, max_row_len=mrl,
+                         chunks=chunks)
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    host_out = torch.full((w.total_tokens, w.nv * w.V), float("nan")).pin_memory()
+    hf(pin(w.qkv), pin(w.decay), pin(w.beta), pin(w.slot_idx), pin(w.offsets), host_out)
+    torch.cuda.synchronize()
+    assert (host_out.numpy().view(np.uint32) == out_ref.view(np.uint32)).all()
+    assert (pool_to_host(state) == pool_ref).all()
+    assert gdr.gdr_get_status() == 0

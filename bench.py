@@ -71,10 +71,12 @@ def peaks():
 
 
 def kernel_source_hash():
+    """Hash of the device code and its launchers (every csrc file but the
+    host-side API layer, api.cu, which checks arguments and picks kernels)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_deltanet_linear_gdr_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
+        if f.endswith((".cu", ".cuh", ".h")) and f != "api.cu":
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

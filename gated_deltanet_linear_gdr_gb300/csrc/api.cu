@@ -182,7 +182,7 @@ cudaError_t launch_fwd(const gdr_step_args *a, unsigned *status, cudaStream_t s)
 }
 
 // Row groups of gdr_fwd_host: the default count and the limit.
-constexpr int kHostChunksAuto = 4;
+constexpr int kHostChunksAuto = 3;
 constexpr int kHostMaxChunks = 16;
 
 // Events that order gdr_fwd_host's copies and kernels across streams: one set
@@ -318,15 +318,19 @@ int gdr_fwd_host(const gdr_step_args *a, const gdr_host_io *h, int32_t chunks, v
     HostEvents *ev = nullptr;
     if ((rc = host_events(&ev))) return rc;
 
-    // groups of consecutive rows with about equal token counts
+    // groups of consecutive rows; with three or more groups the first and the
+    // last get half the tokens of the others, since the first group's copy in
+    // and the last group's copy out are the only copies nothing overlaps
     int nch = chunks > 0 ? chunks : kHostChunksAuto;
     if (nch > kHostMaxChunks) nch = kHostMaxChunks;
     if (nch > a->batch) nch = a->batch;
     int bound[kHostMaxChunks + 1];
     bound[0] = 0;
     const int64_t T0 = off[0], span = (int64_t)off[a->batch] - off[0];
+    const int64_t parts = nch >= 3 ? 2 * nch - 2 : nch;  // in half-group units
     for (int c = 1; c < nch; ++c) {
-        const int64_t target = T0 + span * c / nch;
+        const int64_t upto = nch >= 3 ? 2 * c - 1 : c;      // half-group units before group c
+        const int64_t target = T0 + span * upto / parts;
         int r = bound[c - 1] + 1;  // every group keeps at least one row
         while (r < a->batch - (nch - c) && off[r] < target) ++r;
         bound[c] = r;

@@ -193,8 +193,10 @@ typedef struct gdr_host_io {
  * and out, dense with the shapes above (qkv_seq_stride = 2*nk*K + nv*V,
  * tok_seq_stride = nv, out_seq_stride = nv*V, unit inner strides, head-wise
  * beta) -- and the device pool.  The rows are split into `chunks` groups of
- * consecutive rows with about equal token counts (chunks <= 0: the library
- * picks; at most 16 and at most batch).  Each group's tokens are copied in on
+ * consecutive rows (chunks <= 0: the library picks; at most 16 and at most
+ * batch), with about equal token counts, except that with three or more groups
+ * the first and the last get half as many (their copy in and copy out are the
+ * ones no compute overlaps).  Each group's tokens are copied in on
  * h2d_stream, computed on `stream` and its output copied back on d2h_stream,
  * so one group's copies overlap its neighbours' compute (a NULL side stream
  * puts that direction on `stream`, without overlap).  Asynchronous on

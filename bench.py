@@ -546,9 +546,7 @@ def run_gdr(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {
-            "workload": "decode: batch 256 rows x 1 token (248 live, 8 padding slot -1), nk=16, "
-                        "nv=32, K=V=128, fp32 q/k/v/decay/beta, bf16 state pool "
-                        "[512,32,128,128] at random slots",
+            "workload": DECODE_WORKLOAD,
             "global_batch": 256 * world, "seq_len": 1, "parallelism": f"dp{world}",
             "l2": "flushed before every timed step (read-only sweep of a 2x-L2 buffer)",
             "head_tokens_per_step": ht * world,
@@ -577,6 +575,11 @@ def run_gdr(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+# The headline workload, named the same way by both arms.
+DECODE_WORKLOAD = ("decode: batch 256 rows x 1 token (248 live, 8 padding slot -1), nk=16, nv=32, K=V=128, "
+                   "fp32 q/k/v/decay/beta, bf16 state pool [512,32,128,128] at random slots")
 
 
 def run_reference(args):
@@ -609,9 +612,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": "decode: batch 256 rows x 1 token (248 live, 8 padding slot -1), "
-                               "nk=16, nv=32, K=V=128, bf16 state pool [512,32,128,128]",
-                   "global_batch": 256, "seq_len": 1, "parallelism": "none (CPU oracle)"},
+        "config": {"workload": DECODE_WORKLOAD, "global_batch": 256, "seq_len": 1, "parallelism": "dp1",
+                   "runs_on": "host cores (the CPU oracle)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -61,11 +61,20 @@ __device__ __forceinline__ void tile_issue(const ST *src, long long st_k, uint4 
     constexpr int CPR = Sh::CPR, RPI = NT / CPR, NJ = Sh::S_STATE / NT;
     static_assert(NT % CPR == 0 && Sh::S_STATE % NT == 0, "tile split");
     const int r0 = threadIdx.x / CPR, c0 = threadIdx.x % CPR;
-    src += (long long)r0 * st_k + c0 * (16 / (int)sizeof(ST));
+    // row r0 + j*RPI lands at a per-thread shared base plus a constant per j,
+    // and (when RPI is a multiple of 2^SWS) its swizzle is (r0 >> SWS) plus a
+    // constant per j
+    const unsigned base = (unsigned)__cvta_generic_to_shared(tile) + (unsigned)(r0 * CPR) * 16u;
+    const char *g = reinterpret_cast<const char *>(src + (long long)r0 * st_k + c0 * (16 / (int)sizeof(ST)));
+    const long long gstep = (long long)RPI * st_k * (long long)sizeof(ST);
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-        const int row = r0 + j * RPI;
-        cp_async16(tile + row * CPR + (c0 ^ ((row >> SWS) & (CPR - 1))), src + (long long)j * RPI * st_k);
+        int sw;
+        if constexpr (RPI % (1 << SWS) == 0)
+            sw = ((r0 >> SWS) + j * (RPI >> SWS)) & (CPR - 1);
+        else
+            sw = ((r0 + j * RPI) >> SWS) & (CPR - 1);
+        cp_async16_s(base + (unsigned)(j * RPI * CPR * 16) + (unsigned)(c0 ^ sw) * 16u, g + j * gstep);
     }
 }
 
@@ -84,11 +93,17 @@ __device__ __forceinline__ void tile_store(ST *dst, long long st_k, const uint4 
     using Sh = PipeShape<ST, K, NWMAX>;
     constexpr int CPR = Sh::CPR, RPI = NT / CPR, NJ = Sh::S_STATE / NT;
     const int r0 = threadIdx.x / CPR, c0 = threadIdx.x % CPR;
-    dst += (long long)r0 * st_k + c0 * (16 / (int)sizeof(ST));
+    char *g = reinterpret_cast<char *>(dst + (long long)r0 * st_k + c0 * (16 / (int)sizeof(ST)));
+    const long long gstep = (long long)RPI * st_k * (long long)sizeof(ST);
+    const uint4 *base = tile + r0 * CPR;
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-        const int row = r0 + j * RPI;
-        *reinterpret_cast<uint4 *>(dst + (long long)j * RPI * st_k) = tile[row * CPR + (c0 ^ ((row >> SWS) & (CPR - 1)))];
+        int sw;
+        if constexpr (RPI % (1 << SWS) == 0)
+            sw = ((r0 >> SWS) + j * (RPI >> SWS)) & (CPR - 1);
+        else
+            sw = ((r0 + j * RPI) >> SWS) & (CPR - 1);
+        *reinterpret_cast<uint4 *>(g + j * gstep) = base[j * RPI * CPR + (c0 ^ sw)];
     }
 }
 

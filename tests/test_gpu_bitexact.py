@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import gated_deltanet_linear_gdr_gb300 as gdr
+import gated_deltanet_linear_gdr_gb300._binding as B
 from gated_deltanet_linear_gdr_gb300 import workloads as W
 from tests.gpu_helpers import DEV, Dev, pool_to_dev, pool_to_host, ring_for
 from tests.helpers import sub_workload
@@ -548,3 +549,32 @@ def test_longest_first_block_order_does_not_change_bits():
         t0, t1 = int(w.offsets[b]), int(w.offsets[b + 1])
         assert (o.view(np.uint32) == out[t0:t1].view(np.uint32)).all()
         assert (s1[w.slot_idx[b]] == st[w.slot_idx[b]]).all()
+
+
+def test_host_buffer_forward_single_stream_and_pageable_memory():
+    """gdr_fwd_host through the C ABI with no side streams (everything on one
+    stream) and with pageable (not pinned) host buffers: the same bits as
+    gdr_fwd, and a batch with an empty group of rows."""
+    w = W.random_case(93, [0, 4, 0, 0, 6, 2, 0, 9], nk=2, nv=4, K=32, max_slots=10,
+                      state_dtype="f32", n_pad=1)
+    pool = w.state_pool()
+    out_ref, pool_ref = _run_fwd(w, pool)
+    state = pool_to_dev(pool)
+    hf = gdr.HostForward(state, w.nk, w.batch, w.total_tokens, decay_is_log=w.decay_is_log,
+                         use_qk_l2norm=w.use_l2norm, scale=w.scale, eps=w.eps)
+    lib = gdr.load_library()
+    host = {k: torch.from_numpy(np.ascontiguousarray(v)) for k, v in
+            (("qkv", w.qkv), ("decay", w.decay), ("beta", w.beta), ("slot", w.slot_idx),
+             ("off", w.offsets))}
+    out = torch.full((w.total_tokens, w.nv * w.V), float("nan"))
+    io = B.gdr_host_io(host["qkv"].data_ptr(), host["decay"].data_ptr(), host["beta"].data_ptr(),
+                       host["slot"].data_ptr(), host["off"].data_ptr(), out.data_ptr())
+    stream = torch.cuda.current_stream(DEV).cuda_stream
+    for chunks in (5, 1):
+        out.fill_(float("nan"))
+        state.copy_(pool_to_dev(pool))
+        assert lib.gdr_fwd_host(ctypes.byref(hf.args), ctypes.byref(io), chunks, stream, None, None) == 0
+        torch.cuda.synchronize()
+        assert (out.numpy().view(np.uint32) == out_ref.view(np.uint32)).all(), chunks
+        assert (pool_to_host(state) == pool_ref).all(), chunks
+    assert gdr.gdr_get_status() == 0

@@ -89,6 +89,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                 "gdr_ring_record_elements": ([i32, i32, i32], ctypes.c_int),
                 "gdr_fwd": ([A, vp], ctypes.c_int),
                 "gdr_fwd_host": ([A, ctypes.POINTER(gdr_host_io), i32, vp, vp, vp], ctypes.c_int),
+                "gdr_fwd_host_noalloc": ([A, ctypes.POINTER(gdr_host_io), i32, vp, vp, vp], ctypes.c_int),
                 "gdr_fwd_dense": ([A, vp, vp, vp], ctypes.c_int),
                 "gdr_verify_ring": ([A, vp, i32, i64, i32, i64, vp, vp], ctypes.c_int),
                 "gdr_fold": ([A, vp, i32, i64, i32, i64, vp, vp, vp], ctypes.c_int),

@@ -261,6 +261,41 @@ int check_inter(const gdr_step_args *a, const void *inter, int64_t s_slot, int64
     return GDR_OK;
 }
 
+// ---- device-resident staging for gdr_fwd_host_noalloc ----------------------
+// Some callers cannot allocate device memory at all: code that runs where an
+// allocation would be an error (inside a stream capture with allocation
+// forbidden, under a memory budget owned by someone else, or in a plug-in that
+// only receives host buffers and a stream).  For them the staging buffers of
+// the host-buffer forward pass live in this fixed array, one per device that
+// loads the library, kept until the process exits.
+constexpr size_t kNoAllocScratchBytes = 32u << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_gdr_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+unsigned char *g_noalloc_ptr[64];
+
+// Device address of this device's staging array.  The symbol's name in host
+// code is only a host-side stand-in, so the address is asked for once per
+// device, with that device current, and cached.
+int noalloc_scratch(unsigned char **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(GDR_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_gdr_noalloc_scratch);
+        if (e != cudaSuccess)
+            return fail(GDR_ERR_CUDA, "cudaGetSymbolAddress(staging array): %s", cudaGetErrorString(e));
+        g_noalloc_ptr[dev] = static_cast<unsigned char *>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return GDR_OK;
+}
+
+size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
+
 }  // namespace
 
 extern "C" {
@@ -388,6 +423,54 @@ int gdr_fwd_host(const gdr_step_args *a, const gdr_host_io *h, int32_t chunks, v
     // `stream` passes the call only once every copy back has landed
     if (!order(ds, cs, ev->end)) return fail(GDR_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
     return ok();
+}
+
+int gdr_fwd_host_noalloc(const gdr_step_args *a, const gdr_host_io *h, int32_t chunks, void *stream,
+                         void *h2d_stream, void *d2h_stream) {
+    const char *fn = "gdr_fwd_host_noalloc";
+    if (!a) return fail(GDR_ERR_INVALID_ARG, "%s: args is NULL", fn);
+    if (a->batch < 0 || a->total_tokens < 0 || a->nk <= 0 || a->nv <= 0 || a->K <= 0 || a->V <= 0)
+        return fail(GDR_ERR_INVALID_ARG, "%s: sizes must be positive", fn);
+    // the staging layout: qkv, decay, beta, out, slot_idx, offsets, each 256-byte aligned
+    const int64_t T = a->total_tokens, conv = 2ll * a->nk * a->K + (int64_t)a->nv * a->V;
+    const int64_t ow = (int64_t)a->nv * a->V;
+    const size_t b_qkv = round256((size_t)(T * conv) * sizeof(float));
+    const size_t b_tok = round256((size_t)(T * a->nv) * sizeof(float));
+    const size_t b_out = round256((size_t)(T * ow) * sizeof(float));
+    const size_t b_slot = round256((size_t)a->batch * sizeof(int32_t));
+    const size_t b_off = round256((size_t)(a->batch + 1) * sizeof(int32_t));
+    const size_t need = b_qkv + 2 * b_tok + b_out + b_slot + b_off;
+    if (need > kNoAllocScratchBytes)
+        return fail(GDR_ERR_UNSUPPORTED,
+                    "%s: the call needs %zu bytes of staging, more than the library's fixed %zu-byte array "
+                    "(use gdr_fwd_host with buffers of your own, or fewer tokens per call)",
+                    fn, need, kNoAllocScratchBytes);
+    unsigned char *base = nullptr;
+    int rc = noalloc_scratch(&base);
+    if (rc) return rc;
+    gdr_step_args g = *a;
+    unsigned char *q = base;
+    g.qkv = reinterpret_cast<const float *>(q);
+    g.qkv_seq_stride = conv;
+    g.qkv_chan_stride = 1;
+    q += b_qkv;
+    g.decay = reinterpret_cast<const float *>(q);
+    q += b_tok;
+    g.beta = reinterpret_cast<const float *>(q);
+    q += b_tok;
+    g.tok_seq_stride = a->nv;
+    g.tok_head_stride = 1;
+    g.beta_seq_stride = g.beta_head_stride = g.beta_vdim_stride = 0;
+    g.out = reinterpret_cast<float *>(q);
+    g.out_seq_stride = ow;
+    g.out_vdim_stride = 1;
+    q += b_out;
+    g.slot_idx = reinterpret_cast<const int32_t *>(q);
+    q += b_slot;
+    g.offsets = reinterpret_cast<const int32_t *>(q);
+    // every staged byte a call reads is written by that call's own copies
+    // first, so nothing needs clearing between calls
+    return gdr_fwd_host(&g, h, chunks, stream, h2d_stream, d2h_stream);
 }
 
 int gdr_fwd_dense(const gdr_step_args *a, const void *initial_state, void *final_state, void *stream) {

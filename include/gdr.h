@@ -210,6 +210,28 @@ typedef struct gdr_host_io {
 int gdr_fwd_host(const gdr_step_args *args, const gdr_host_io *host, int32_t chunks, void *stream,
                  void *h2d_stream, void *d2h_stream);
 
+/* gdr_fwd_host without any device buffers from the caller.  (The pages have
+ * no counterpart: this is an entry point for callers that cannot allocate.)
+ * Some callers cannot call cudaMalloc or any other allocator: code running
+ * where an allocation is not allowed or not wanted (a plug-in that is handed
+ * host buffers and a stream only, a stream capture that forbids allocation,
+ * a process whose device memory budget belongs to someone else).  This entry
+ * point stages the tokens and the output in one fixed device array that the
+ * library defines statically: 32 MiB on every GPU that loads the library,
+ * held until the process exits.  `args` is read as for gdr_fwd_host except
+ * that its qkv, decay, beta, slot_idx, offsets and out pointers and strides
+ * are ignored (the library places dense copies in its array); the pool is the
+ * caller's, on the device, as always.  A call whose staging would exceed the
+ * array (about 4 * T * (2*nk*K + 2*nv*V + 2*nv) bytes) returns
+ * GDR_ERR_UNSUPPORTED without launching anything.  Nothing is allocated: the
+ * first call on a device looks up the array's device address (keep that first
+ * call out of any stream capture); later calls reuse it.  Every call on a
+ * device shares the one array and each call overwrites what it reads, so
+ * calls that overlap on the GPU (on different streams, or from several host
+ * threads without ordering) race: order them on one stream. */
+int gdr_fwd_host_noalloc(const gdr_step_args *args, const gdr_host_io *host, int32_t chunks, void *stream,
+                         void *h2d_stream, void *d2h_stream);
+
 /* Forward pass with a dense start and end state ("core.ssm.ops.gdp.fused_recurrent",
  * initial_state [N, HV, K, V] or None for zeros, output_final_state): as gdr_fwd,
  * but row b starts from initial_state[b] (zeros when initial_state is NULL) and

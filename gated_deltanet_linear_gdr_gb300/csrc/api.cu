@@ -431,6 +431,8 @@ int gdr_fwd_host_noalloc(const gdr_step_args *a, const gdr_host_io *h, int32_t c
     if (!a) return fail(GDR_ERR_INVALID_ARG, "%s: args is NULL", fn);
     if (a->batch < 0 || a->total_tokens < 0 || a->nk <= 0 || a->nv <= 0 || a->K <= 0 || a->V <= 0)
         return fail(GDR_ERR_INVALID_ARG, "%s: sizes must be positive", fn);
+    if (a->beta_vdim_stride > 0)
+        return fail(GDR_ERR_UNSUPPORTED, "%s: beta must be [total_tokens, nv] (beta_vdim_stride 0)", fn);
     // the staging layout: qkv, decay, beta, out, slot_idx, offsets, each 256-byte aligned
     const int64_t T = a->total_tokens, conv = 2ll * a->nk * a->K + (int64_t)a->nv * a->V;
     const int64_t ow = (int64_t)a->nv * a->V;

@@ -284,3 +284,24 @@ def test_fwd_host_rejects_bad_arguments(lib):
     a = _valid_args()
     a.batch = 0
     assert call(a, ctypes.byref(io)) == B.GDR_OK
+
+
+def test_fwd_host_noalloc_rejects_bad_arguments(lib):
+    """Checks of gdr_fwd_host_noalloc that come before its device set-up."""
+    fake = 0x7f0000000000
+    off = (ctypes.c_int32 * 3)(0, 5, 8)
+    io = B.gdr_host_io(fake, fake, fake, fake, ctypes.addressof(off), fake)
+    call = lambda a: lib.gdr_fwd_host_noalloc(ctypes.byref(a) if a is not None else None,
+                                              ctypes.byref(io), 0, None, None, None)
+    assert call(None) == B.GDR_ERR_INVALID_ARG
+    a = _valid_args()
+    a.nv = 0
+    assert call(a) == B.GDR_ERR_INVALID_ARG
+    a = _valid_args()
+    a.beta_seq_stride, a.beta_head_stride, a.beta_vdim_stride = 64, 16, 1
+    assert call(a) == B.GDR_ERR_UNSUPPORTED
+    a = _valid_args()
+    a.total_tokens = 1 << 20  # far beyond the library's staging array
+    assert call(a) == B.GDR_ERR_UNSUPPORTED
+    assert b"staging" in lib.gdr_last_error()
+

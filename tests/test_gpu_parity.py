@@ -371,3 +371,50 @@ def test_snapshot_small_bf16_against_oracle():
     check_out(out, ref)
     check_state(pool_to_host(inter), oint)
     check_state(pool_to_host(d.state), p.state)
+
+
+@pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
+def test_limits_ring_len_32_and_64_token_rows(state_dtype):
+    """The largest ring (RING_LEN 32) with rows of exactly 32 tokens (they
+    record) and 33 and 64 (they commit like the forward pass), the latter at
+    the short-row kernel's 64-token limit: verify against the oracle through
+    both kernels, which agree bit for bit, then fold against the oracle's fold."""
+    lengths = [32, 33, 64, 1, 17, 0]
+    w = W.random_case(713, lengths, nk=2, nv=4, K=64, max_slots=8, state_dtype=state_dtype, n_pad=0)
+    pool = w.state_pool()
+    ring_len, rows = 32, w.batch
+    rsi_np = np.arange(w.batch, dtype=np.int32)[::-1].copy()
+    rsi = torch.from_numpy(rsi_np).to(DEV)
+    pv = problem(w, state=pool.copy())
+    oring = np.full((rows, w.nk, ring_len, ring_for(w, ring_len, rows).shape[3]), np.nan, np.float32)
+    ref = oracle.verify_ring(pv, oring, rsi_np, ring_len)
+    got = []
+    for hint in (64, 0):
+        d = Dev(w, pool)
+        ring = ring_for(w, ring_len, rows)
+        out = d.verify(ring, rsi, max_row_len=hint)
+        torch.cuda.synchronize()
+        check_out(out, ref)
+        host = pool_to_host(d.state)
+        for b, L in enumerate(lengths):
+            s = int(w.slot_idx[b])
+            if L > ring_len:
+                check_state(host, pv.state, slots=[s])
+            else:
+                assert (host[s] == pool[s]).all(), b
+        g = ring.cpu().numpy()
+        assert (np.isnan(g) == np.isnan(oring)).all()
+        m = ~np.isnan(oring)
+        np.testing.assert_allclose(g[m], oring[m], rtol=1e-4, atol=1e-4)
+        got.append((out.cpu().numpy(), g, host, d, ring))
+    assert (got[0][0].view(np.uint32) == got[1][0].view(np.uint32)).all()
+    m = ~np.isnan(got[0][1])
+    assert (got[0][1][m].view(np.uint32) == got[1][1][m].view(np.uint32)).all()
+    assert (got[0][2] == got[1][2]).all()
+    counts = np.array([32, 33, 64, 1, 9, 0], np.int32)
+    _, _, _, d, ring = got[0]
+    gdr.gdr_fold(d.state, d.slot, ring, rsi, torch.from_numpy(counts).to(DEV))
+    torch.cuda.synchronize()
+    oracle.fold(pv, oring, rsi_np, counts, ring_len)
+    check_state(pool_to_host(d.state), pv.state, slots=w.live_slots())
+    assert gdr.gdr_get_status(clear=True) == 0

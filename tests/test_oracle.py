@@ -92,6 +92,44 @@ def test_matches_matrix_form_bruteforce_k_ne_v(KV):
         np.testing.assert_allclose(p.state[s, h], S, rtol=1e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("seed", range(16))
+def test_random_shapes_match_matrix_form_bruteforce(seed):
+    """A sweep over small random shapes and options: key/value head counts with
+    GQA groups of 1, 2 or 4, K from 2 to 16, V = K or 2K, ragged row lengths
+    including empty rows, padding rows, either decay form, with or without the
+    L2 norm, default or explicit scale.  Each draw is checked against the
+    matrix-form step ("core.ssm.ops.gdp.fused_recurrent")."""
+    rng = np.random.default_rng(1000 + seed)
+    nk = int(rng.choice([1, 2]))
+    nv = nk * int(rng.choice([1, 2, 4]))
+    K = int(rng.choice([2, 4, 8, 16]))
+    V = K * int(rng.choice([1, 2]))
+    lengths = [int(x) for x in rng.integers(0, 7, size=int(rng.integers(1, 6)))]
+    n_pad = int(rng.integers(0, len(lengths)))
+    log = bool(rng.integers(0, 2))
+    l2 = bool(rng.integers(0, 2))
+    scale = float(rng.choice([0.0, 0.37]))
+    w = _small(2000 + seed, lengths, nk=nk, nv=nv, K=K, V=V, n_pad=n_pad, decay_is_log=log,
+               use_l2norm=l2, scale=scale)
+    pool = w.state_pool()
+    p = problem(w, state=pool.copy())
+    out = oracle.fwd(p)
+    ref_out, finals = brute.fwd(w.qkv, w.decay, w.beta, pool, w.slot_idx, w.offsets,
+                                nk=nk, nv=nv, K=K, V=V, decay_is_log=log, use_l2norm=l2,
+                                scale=scale, eps=w.eps)
+    np.testing.assert_allclose(out, ref_out, rtol=1e-10, atol=1e-12)
+    touched = set()
+    for (s, h), S in finals.items():
+        touched.add((s, h))
+        # the pool stores float32: the oracle's state is the float32 rounding of its
+        # float64 state, which agrees with the matrix form to well under float32 ulp
+        np.testing.assert_allclose(p.state[s, h], S, rtol=1e-6, atol=1e-7)
+    for s in range(pool.shape[0]):
+        for h in range(nv):
+            if (s, h) not in touched:
+                assert (p.state[s, h] == pool[s, h]).all()
+
+
 def test_value_columns_split_into_independent_halves():
     """The value columns never mix: a V = 2K run equals, exactly, two V = K runs
     on the two halves of the value columns (v, state and output split alike)."""

@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/gdr.h"
 
 namespace gdr {
@@ -110,6 +113,45 @@ struct FastDiv {
     }
 #endif
 };
+
+// Per-device facts a launcher looks up once: the SM count and what its init
+// callback fills in (resident CTAs per SM; the callback also opts the kernel
+// into its dynamic shared memory).  The first caller on a device fills them in
+// under the mutex and publishes them with a release store; later callers, on
+// any thread, read `ready` with acquire and so see complete values.  A failed
+// init publishes nothing and is retried by the next call.
+constexpr int kMaxDevices = 64;
+struct LaunchInfo {
+    int sms, occ;
+};
+struct LaunchCache {
+    std::atomic<int> ready[kMaxDevices];  // zero-initialised: instances are static
+    LaunchInfo info[kMaxDevices];
+    std::mutex mu;
+};
+
+template <typename Init>
+inline cudaError_t launch_info(LaunchCache &c, LaunchInfo *out, Init &&init) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!c.ready[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lk(c.mu);
+        if (!c.ready[dev].load(std::memory_order_relaxed)) {
+            LaunchInfo li{0, 1};
+            e = cudaDeviceGetAttribute(&li.sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e == cudaSuccess) e = init(li);
+            if (e != cudaSuccess) return e;
+            if (li.sms < 1) li.sms = 1;
+            if (li.occ < 1) li.occ = 1;
+            c.info[dev] = li;
+            c.ready[dev].store(1, std::memory_order_release);
+        }
+    }
+    *out = c.info[dev];
+    return cudaSuccess;
+}
 
 // Launchers (defined next to their kernels).  Return cudaGetLastError().
 cudaError_t launch_decode(const StepParams &p, int K, bool bf16, cudaStream_t s);

@@ -357,21 +357,15 @@ template <typename ST, int K, int V, Mode MODE, bool BPV, int TCX>
 inline cudaError_t launch_chain_k(const StepParams &p, const RingParams &rp, const SnapParams &sp,
                                   long long max_len, long long blocks, cudaStream_t st) {
     using Sh = ChainShape<ST, K, V, BPV, TCX>;
-    static int configured[64] = {0}, sms[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static LaunchCache cache;
+    LaunchInfo li;
+    cudaError_t e = launch_info(cache, &li, [](LaunchInfo &) {
+        return cudaFuncSetAttribute(k_chain<ST, K, V, MODE, BPV, TCX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Sh::SMEM);
+    });
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(k_chain<ST, K, V, MODE, BPV, TCX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Sh::SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        configured[dev] = 1;
-    }
     // a few rows: deal them out longest first (chain_balanced_unit)
-    const int order_p = (p.batch <= Sh::NT && p.batch <= kChainOrderRows && blocks > sms[dev]) ? sms[dev] : 0;
+    const int order_p = (p.batch <= Sh::NT && p.batch <= kChainOrderRows && blocks > li.sms) ? li.sms : 0;
     k_chain<ST, K, V, MODE, BPV, TCX><<<(unsigned)blocks, Sh::NT, Sh::SMEM, st>>>(p, rp, sp, max_len, order_p);
     return cudaGetLastError();
 }

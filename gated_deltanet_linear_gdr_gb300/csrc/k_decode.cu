@@ -340,24 +340,16 @@ template <typename ST, int K> static cudaError_t launch_pipe_t(const StepParams 
     using Sh = PipeShape<ST, K, kDecodeWarps>;
     constexpr int NS = kDecodeStages;
     constexpr int SMEM = NS * Sh::SMEM1;
-    static int configured[64] = {0};
-    static int sms[64] = {0}, occ[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static LaunchCache cache;
+    LaunchInfo li;
+    cudaError_t e = launch_info(cache, &li, [](LaunchInfo &x) {
+        cudaError_t r = cudaFuncSetAttribute(k_decode_pipe<ST, K, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (r != cudaSuccess) return r;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&x.occ, k_decode_pipe<ST, K, NS>, Sh::NT, SMEM);
+    });
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(k_decode_pipe<ST, K, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[dev], k_decode_pipe<ST, K, NS>, Sh::NT, SMEM);
-        if (e != cudaSuccess) return e;
-        if (occ[dev] < 1) occ[dev] = 1;
-        configured[dev] = 1;
-    }
     const long long nunits = (long long)p.batch * p.nv * Sh::USL;
-    long long grid = (long long)sms[dev] * occ[dev];
+    long long grid = (long long)li.sms * li.occ;
     if (grid > nunits) grid = nunits;
     if (grid > 0) k_decode_pipe<ST, K, NS><<<(unsigned)grid, Sh::NT, SMEM, st>>>(p, (int)nunits);
     return cudaGetLastError();

@@ -370,24 +370,16 @@ static cudaError_t launch_short_m(const StepParams &p, const RingParams &rp, con
     using P = ShortTile<ST, K>;
     using W = WinShape<ST, K>;
     constexpr int SMEM = 2 * W::SMEM1;
-    static int configured[64] = {0};
-    static int sms[64] = {0}, occ[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static LaunchCache cache;
+    LaunchInfo li;
+    cudaError_t e = launch_info(cache, &li, [](LaunchInfo &x) {
+        cudaError_t r = cudaFuncSetAttribute(k_short<ST, K, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (r != cudaSuccess) return r;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&x.occ, k_short<ST, K, MODE>, W::NT, SMEM);
+    });
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(k_short<ST, K, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[dev], k_short<ST, K, MODE>, W::NT, SMEM);
-        if (e != cudaSuccess) return e;
-        if (occ[dev] < 1) occ[dev] = 1;
-        configured[dev] = 1;
-    }
     const long long nunits = (long long)p.batch * p.nv * P::USL;
-    long long grid = (long long)sms[dev] * occ[dev];
+    long long grid = (long long)li.sms * li.occ;
     if (grid > nunits) grid = nunits;
     if (grid > 0)
         k_short<ST, K, MODE><<<(unsigned)grid, W::NT, SMEM, st>>>(p, rp, sp, max_len, (int)nunits,

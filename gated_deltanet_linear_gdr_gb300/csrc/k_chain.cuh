@@ -3,7 +3,7 @@
 // A CTA owns one (row, value head, slice of VS value columns) for the whole
 // row and keeps its K x VS piece of the state in registers in float32
 // ("gated_delta_recurrence_fwd_gpu" summary: the state stays in registers for
-// the whole sequence).  Each warp owns 16 of the columns and all K rows:
+// the whole sequence).  Each warp owns WC of the columns and all K rows:
 // lane kl = lane % LK holds RG consecutive row groups (8*RG rows, in the
 // row-pair form of gdr_state.cuh when RG is even), lane vl = lane / LK holds
 // C columns.  The K-reductions of a token therefore end
@@ -28,7 +28,14 @@ namespace gdr {
 template <typename ST, int K, int VV = K, bool BPV = false, int TCX = 16> struct ChainShape {
     static constexpr int V = VV;                   // value head size: K or 2K
     static constexpr int NG = K / 8;               // row groups
-    static constexpr int LK = NG >= 4 ? cmin(4, NG / 2) : NG;  // lanes along K
+    // lanes along K: 4 (32 rows per lane at K = 128), or 2 for K = 128 with
+    // 32-token chunks.  Long rows run one CTA per row and head for the whole
+    // row, so the work a lane carries per token sets how well two CTAs per SM
+    // keep the FMA pipes busy: 64 rows per lane (a whole-head CTA, 213
+    // registers) beat 32 rows (ragged prefill 2.02 -> 1.90 ms) and 16 rows
+    // (2.32 ms).  Rows bounded at 8 or 16 tokens keep the narrower lane, whose
+    // CTAs fit four to an SM.
+    static constexpr int LK = (NG >= 16 && TCX >= 32 && !BPV) ? 2 : NG >= 4 ? cmin(4, NG / 2) : NG;
     static constexpr int RG = NG / LK;             // groups per lane
     static constexpr bool RPAIR = RG % 2 == 0;     // row-pair register form
     static constexpr int ROWS = RG * 8;            // rows per lane
@@ -85,9 +92,10 @@ __device__ __forceinline__ long long chain_balanced_unit(const StepParams &p, in
     return (long long)row_of_rank * per_row + (k - (long long)rank * per_row);
 }
 
-// 32-token chunks take 91 KiB of shared memory at K = V = 128, so two CTAs
-// fit an SM anyway: the register cap follows (the extra registers let the
-// compiler keep more staged operands in flight; ragged prefill 2.10 -> 2.02 ms).
+// 32-token chunks take 101 KiB of shared memory at K = 128, so two CTAs fit
+// an SM anyway: the register cap follows (the 64-row lane needs the extra
+// registers; with 32-row lanes they already let the compiler keep more staged
+// operands in flight, ragged prefill 2.10 -> 2.02 ms).
 template <typename ST, int K, int VV, Mode MODE, bool BPV, int TCX>
 __global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX>::NT, TCX >= 32 ? 2 : 4)
     k_chain(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len, const int order_p) {
@@ -344,7 +352,7 @@ constexpr int kChainLongTC = 32;
 constexpr int kChainOrderRows = 32;
 
 // The launchers of each pass (one translation unit each, so they compile in
-// parallel); blocks = batch * nv * SLICES.
+// parallel).
 cudaError_t launch_chain_fwd(const StepParams &p, int K, int V, bool bf16, long long max_len, cudaStream_t st);
 cudaError_t launch_chain_verify(const StepParams &p, int K, bool bf16, const RingParams &rp, long long max_len,
                                 cudaStream_t st);
@@ -352,11 +360,14 @@ cudaError_t launch_chain_snap(const StepParams &p, int K, int V, bool bf16, cons
                               cudaStream_t st);
 
 // Launches one instantiation with its dynamic shared memory (opted in once per
-// device above 48 KiB).
+// device above 48 KiB); blocks = batch * nv * SLICES of that instantiation.
 template <typename ST, int K, int V, Mode MODE, bool BPV, int TCX>
 inline cudaError_t launch_chain_k(const StepParams &p, const RingParams &rp, const SnapParams &sp,
-                                  long long max_len, long long blocks, cudaStream_t st) {
+                                  long long max_len, cudaStream_t st) {
     using Sh = ChainShape<ST, K, V, BPV, TCX>;
+    const long long blocks = (long long)p.batch * p.nv * Sh::SLICES;
+    if (blocks <= 0) return cudaGetLastError();
+    if (blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
     static LaunchCache cache;
     LaunchInfo li;
     cudaError_t e = launch_info(cache, &li, [](LaunchInfo &) {

@@ -5,19 +5,16 @@ namespace gdr {
 
 template <typename ST, int K, int V>
 static cudaError_t fwd_t(const StepParams &p, long long max_len, cudaStream_t st) {
-    const long long blocks = (long long)p.batch * p.nv * ChainShape<ST, K, V>::SLICES;
-    if (blocks <= 0) return cudaGetLastError();
-    static_assert(ChainShape<ST, K, V, true, 8>::SLICES == ChainShape<ST, K, V>::SLICES, "same grid");
     const RingParams rp{};
     const SnapParams sp{};
     // chunk tokens: rows bounded at 8 or 16 tokens get chunks of that size (a
     // smaller stage, more L1); longer or unbounded rows take kChainLongTC
     // (fewer chunk barriers and normalisation passes per token)
-    if (p.bpv) return launch_chain_k<ST, K, V, Mode::Fwd, true, 8>(p, rp, sp, max_len, blocks, st);
-    if (max_len >= 1 && max_len <= 8) return launch_chain_k<ST, K, V, Mode::Fwd, false, 8>(p, rp, sp, max_len, blocks, st);
+    if (p.bpv) return launch_chain_k<ST, K, V, Mode::Fwd, true, 8>(p, rp, sp, max_len, st);
+    if (max_len >= 1 && max_len <= 8) return launch_chain_k<ST, K, V, Mode::Fwd, false, 8>(p, rp, sp, max_len, st);
     if (max_len >= 1 && max_len <= 16)
-        return launch_chain_k<ST, K, V, Mode::Fwd, false, 16>(p, rp, sp, max_len, blocks, st);
-    return launch_chain_k<ST, K, V, Mode::Fwd, false, kChainLongTC>(p, rp, sp, max_len, blocks, st);
+        return launch_chain_k<ST, K, V, Mode::Fwd, false, 16>(p, rp, sp, max_len, st);
+    return launch_chain_k<ST, K, V, Mode::Fwd, false, kChainLongTC>(p, rp, sp, max_len, st);
 }
 
 cudaError_t launch_chain_fwd(const StepParams &p, int K, int V, bool bf16, long long max_len, cudaStream_t st) {

@@ -5,12 +5,10 @@ namespace gdr {
 
 template <typename ST, int K, int V>
 static cudaError_t snap_t(const StepParams &p, const SnapParams &sp, long long max_len, cudaStream_t st) {
-    const long long blocks = (long long)p.batch * p.nv * ChainShape<ST, K, V>::SLICES;
-    if (blocks <= 0) return cudaGetLastError();
     const RingParams rp{};
-    if (p.bpv) return launch_chain_k<ST, K, V, Mode::Snap, true, 8>(p, rp, sp, max_len, blocks, st);
-    if (max_len >= 1 && max_len <= 8) return launch_chain_k<ST, K, V, Mode::Snap, false, 8>(p, rp, sp, max_len, blocks, st);
-    return launch_chain_k<ST, K, V, Mode::Snap, false, 16>(p, rp, sp, max_len, blocks, st);
+    if (p.bpv) return launch_chain_k<ST, K, V, Mode::Snap, true, 8>(p, rp, sp, max_len, st);
+    if (max_len >= 1 && max_len <= 8) return launch_chain_k<ST, K, V, Mode::Snap, false, 8>(p, rp, sp, max_len, st);
+    return launch_chain_k<ST, K, V, Mode::Snap, false, 16>(p, rp, sp, max_len, st);
 }
 
 cudaError_t launch_chain_snap(const StepParams &p, int K, int V, bool bf16, const SnapParams &sp, long long max_len,

@@ -5,10 +5,8 @@ namespace gdr {
 
 template <typename ST, int K>
 static cudaError_t verify_t(const StepParams &p, const RingParams &rp, long long max_len, cudaStream_t st) {
-    const long long blocks = (long long)p.batch * p.nv * ChainShape<ST, K, K>::SLICES;
-    if (blocks <= 0) return cudaGetLastError();
     if (p.bpv) return cudaErrorInvalidValue;
-    return launch_chain_k<ST, K, K, Mode::Verify, false, 16>(p, rp, SnapParams{}, max_len, blocks, st);
+    return launch_chain_k<ST, K, K, Mode::Verify, false, 16>(p, rp, SnapParams{}, max_len, st);
 }
 
 cudaError_t launch_chain_verify(const StepParams &p, int K, bool bf16, const RingParams &rp, long long max_len,

@@ -29,13 +29,15 @@ template <typename ST, int K, int VV = K, bool BPV = false, int TCX = 16> struct
     static constexpr int V = VV;                   // value head size: K or 2K
     static constexpr int NG = K / 8;               // row groups
     // lanes along K: 4 (32 rows per lane at K = 128), or 2 for K = 128 with
-    // 32-token chunks.  Long rows run one CTA per row and head for the whole
-    // row, so the work a lane carries per token sets how well two CTAs per SM
-    // keep the FMA pipes busy: 64 rows per lane (a whole-head CTA, 213
-    // registers) beat 32 rows (ragged prefill 2.02 -> 1.90 ms) and 16 rows
-    // (2.32 ms).  Rows bounded at 8 or 16 tokens keep the narrower lane, whose
-    // CTAs fit four to an SM.
-    static constexpr int LK = (NG >= 16 && TCX >= 32 && !BPV) ? 2 : NG >= 4 ? cmin(4, NG / 2) : NG;
+    // 32-token chunks or a float32 state.  Long rows run one CTA per row and
+    // head for the whole row, so the work a lane carries per token sets how
+    // well two CTAs per SM keep the FMA pipes busy: 64 rows per lane (a
+    // whole-head CTA, 213 registers) beat 32 rows (ragged prefill 2.02 -> 1.90
+    // ms) and 16 rows (2.32 ms).  Float32 snapshots gain too (154 -> 146 us:
+    // each warp store covers 128 contiguous bytes of a row).  bf16 rows bounded
+    // at 8 or 16 tokens keep the narrower lane, whose CTAs fit four to an SM.
+    static constexpr int LK =
+        (NG >= 16 && (TCX >= 32 || sizeof(ST) == 4) && !BPV) ? 2 : NG >= 4 ? cmin(4, NG / 2) : NG;
     static constexpr int RG = NG / LK;             // groups per lane
     static constexpr bool RPAIR = RG % 2 == 0;     // row-pair register form
     static constexpr int ROWS = RG * 8;            // rows per lane
@@ -95,9 +97,11 @@ __device__ __forceinline__ long long chain_balanced_unit(const StepParams &p, in
 // 32-token chunks take 101 KiB of shared memory at K = 128, so two CTAs fit
 // an SM anyway: the register cap follows (the 64-row lane needs the extra
 // registers; with 32-row lanes they already let the compiler keep more staged
-// operands in flight, ragged prefill 2.10 -> 2.02 ms).
+// operands in flight, ragged prefill 2.10 -> 2.02 ms).  The 64-row lane takes
+// the same cap with shorter chunks.
 template <typename ST, int K, int VV, Mode MODE, bool BPV, int TCX>
-__global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX>::NT, TCX >= 32 ? 2 : 4)
+__global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX>::NT,
+                                  (TCX >= 32 || ChainShape<ST, K, VV, BPV, TCX>::ROWS >= 64) ? 2 : 4)
     k_chain(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len, const int order_p) {
     using Sh = ChainShape<ST, K, VV, BPV, TCX>;
     constexpr int V = VV, LK = Sh::LK, ROWS = Sh::ROWS, C = Sh::C;

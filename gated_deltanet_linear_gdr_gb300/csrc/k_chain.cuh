@@ -37,7 +37,7 @@ template <typename ST, int K, int VV = K, bool BPV = false, int TCX = 16> struct
     // each warp store covers 128 contiguous bytes of a row).  bf16 rows bounded
     // at 8 or 16 tokens keep the narrower lane, whose CTAs fit four to an SM.
     static constexpr int LK =
-        (NG >= 16 && (TCX >= 32 || sizeof(ST) == 4) && !BPV) ? 2 : NG >= 4 ? cmin(4, NG / 2) : NG;
+        (NG >= 16 && ((TCX >= 32 && !BPV) || sizeof(ST) == 4)) ? 2 : NG >= 4 ? cmin(4, NG / 2) : NG;
     static constexpr int RG = NG / LK;             // groups per lane
     static constexpr bool RPAIR = RG % 2 == 0;     // row-pair register form
     static constexpr int ROWS = RG * 8;            // rows per lane

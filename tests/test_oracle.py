@@ -677,6 +677,51 @@ def test_fold_equals_forward_over_accepted_prefix_bitwise_float32(state_dtype):
         assert (pv.state[s] == pf.state[s]).all(), (b, c)
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_random_verify_fold_equals_prefix_forward(seed):
+    """The same contract over random small shapes: GQA groups of 1 or 2, K from
+    4 to 16, either decay form, either pool type, ragged rows around RING_LEN,
+    accepted counts from 0 to the row's length, rows in shuffled ring rows."""
+    rng = np.random.default_rng(3000 + seed)
+    nk = int(rng.choice([1, 2]))
+    nv = nk * int(rng.choice([1, 2]))
+    K = int(rng.choice([4, 8, 16]))
+    ring_len = int(rng.choice([2, 4, 8]))
+    lengths = [int(x) for x in rng.integers(0, ring_len + 3, size=int(rng.integers(2, 7)))]
+    state_dtype = str(rng.choice(["f32", "bf16"]))
+    log = bool(rng.integers(0, 2))
+    w = _small(4000 + seed, lengths, nk=nk, nv=nv, K=K, state_dtype=state_dtype,
+               n_pad=int(rng.integers(0, 2)), decay_is_log=log)
+    # an accepted count is at most the row's length; a row longer than RING_LEN
+    # is committed by the verify pass and recorded nothing, so its count is past
+    # RING_LEN (the fold must skip it)
+    counts = np.array([L if L > ring_len else int(rng.integers(0, L + 1)) for L in lengths],
+                      np.int32)
+    rsi = rng.permutation(w.batch).astype(np.int32)
+    pool = w.state_pool()
+    pv = problem(w, state=pool.copy())
+    ring = _ring(w, w.nk, ring_len, w.batch)
+    oracle.verify_ring(pv, ring, rsi, ring_len, work="f32")
+    oracle.fold(pv, ring, rsi, counts, ring_len, work="f32")
+    for b in range(w.batch):
+        s = int(w.slot_idx[b])
+        if s < 0:
+            continue
+        L, c = int(w.row_lengths[b]), int(counts[b])
+        # rows longer than RING_LEN commit in the verify pass; the fold skips
+        # counts of zero or past RING_LEN; otherwise the first c tokens count
+        n = L if L > ring_len else (c if 0 < c <= ring_len else 0)
+        if n == 0:
+            assert (pv.state[s] == pool[s]).all(), (b, L, c)
+            continue
+        pref = sub_workload(w, [b])
+        pref = dataclasses.replace(pref, offsets=np.array([0, n], np.int32),
+                                   qkv=pref.qkv[:n], decay=pref.decay[:n], beta=pref.beta[:n])
+        pf = problem(pref, state=pool.copy())
+        oracle.fwd(pf, work="f32")
+        assert (pv.state[s] == pf.state[s]).all(), (b, L, c)
+
+
 def test_fold_float64_close_to_prefix_forward():
     w = _small(24, [5, 5], nk=1, nv=2, K=16, state_dtype="f32")
     counts = np.array([2, 5], np.int32)

@@ -814,6 +814,48 @@ def test_snapshots_equal_prefix_forward_and_rollback(state_dtype):
         assert (pr.state[s] == inter[s, acc[b]]).all()
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_random_snapshots_equal_prefix_forward(seed):
+    """The snapshot contract over random small shapes: steps per token 1 to 3,
+    2 to 4 snapshot slots, rows that end mid-draft or hold fewer drafts than
+    the slots, either pool type and decay form."""
+    rng = np.random.default_rng(5000 + seed)
+    nk = int(rng.choice([1, 2]))
+    nv = nk * int(rng.choice([1, 2]))
+    K = int(rng.choice([4, 8]))
+    spt = int(rng.integers(1, 4))
+    drafts = int(rng.integers(2, 5))
+    lengths = [int(x) for x in rng.integers(0, drafts * spt + 1, size=int(rng.integers(2, 6)))]
+    state_dtype = str(rng.choice(["f32", "bf16"]))
+    w = _small(6000 + seed, lengths, nk=nk, nv=nv, K=K, state_dtype=state_dtype,
+               n_pad=int(rng.integers(0, 2)), decay_is_log=bool(rng.integers(0, 2)))
+    pool = w.state_pool()
+    dt = pool.dtype
+    blank = 0xFFFF if dt == np.uint16 else np.nan
+    inter = np.full((w.max_slots, drafts, w.nv, w.K, w.V), blank, dtype=dt)
+    ps = problem(w, state=pool.copy())
+    oracle.fwd_snapshots(ps, inter, spt)
+    for b in range(w.batch):
+        s = int(w.slot_idx[b])
+        if s < 0:
+            continue
+        L = int(w.row_lengths[b])
+        for i in range(drafts):
+            n = (i + 1) * spt
+            if n > L:  # not reached: nothing written
+                if dt == np.uint16:
+                    assert (inter[s, i] == blank).all()
+                else:
+                    assert np.isnan(inter[s, i]).all()
+                continue
+            pref = sub_workload(w, [b])
+            pref = dataclasses.replace(pref, offsets=np.array([0, n], np.int32),
+                                       qkv=pref.qkv[:n], decay=pref.decay[:n], beta=pref.beta[:n])
+            pp = problem(pref, state=pool.copy())
+            oracle.fwd(pp)
+            assert (inter[s, i] == pp.state[s]).all(), (b, i)
+
+
 def test_gdp_config_folding_structure():
     """Config-5 input structure: decay only on the first Householder copy."""
     w = W.gdp_snapshots(batch=2, nk=1, nv=2, K=16, max_slots=4)

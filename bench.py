@@ -147,7 +147,9 @@ class ClockSampler:
 # ------------------------------------------------------------- workloads ---
 
 def decode_bytes(w, sb):
-    """Algorithmic HBM bytes of one decode/forward call."""
+    """Algorithmic HBM bytes of one decode/forward call: each live row's state
+    read and written once, each live token's q, k, v, decay, beta read and its
+    output written, a padding token's zeroed output, and the index arrays."""
     conv = 2 * w.nk * w.K + w.nv * w.V
     live = w.slot_idx >= 0
     L = w.row_lengths

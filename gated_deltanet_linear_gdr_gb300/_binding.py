@@ -361,6 +361,10 @@ def _inter_strides(inter, state):
         raise TypeError("intermediate_states must have the pool's dtype")
     if inter.dim() != 5 or inter.shape[2:] != state.shape[1:]:
         raise ValueError("intermediate_states must be [slots, n_inter, nv, K, V]")
+    if inter.shape[0] < state.shape[0]:
+        # the kernels index it by pool slot, which is only checked against the pool's slot count
+        raise ValueError(f"intermediate_states has {inter.shape[0]} slot rows; it needs one per pool "
+                         f"slot ({state.shape[0]})")
     K, V = state.shape[2:]
     if inter.stride(4) != 1 or inter.stride(3) != V:
         raise ValueError("each [K, V] block of intermediate_states must be dense")

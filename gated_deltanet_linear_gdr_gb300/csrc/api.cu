@@ -68,8 +68,8 @@ int check_pool(const gdr_step_args *a, const char *fn) {
         return fail(GDR_ERR_INVALID_ARG, "%s: nv=%d, nk=%d must be positive", fn, a->nv, a->nk);
     if (a->nv % a->nk != 0)
         return fail(GDR_ERR_INVALID_ARG, "%s: nv=%d is not a multiple of nk=%d", fn, a->nv, a->nk);
-    if (a->V != a->K && a->V != 2 * a->K)
-        return fail(GDR_ERR_UNSUPPORTED, "%s: V=%d must be K=%d or 2K", fn, a->V, a->K);
+    if (a->V != a->K && a->V != 2 * a->K && !(2 * a->V == a->K && a->K >= 32))
+        return fail(GDR_ERR_UNSUPPORTED, "%s: V=%d must be K=%d, 2K, or K/2 with K >= 32", fn, a->V, a->K);
     if (!supported_dim(a->K))
         return fail(GDR_ERR_UNSUPPORTED, "%s: K=%d not in {16,32,64,128}", fn, a->K);
     if (a->state_dtype != GDR_F32 && a->state_dtype != GDR_BF16)

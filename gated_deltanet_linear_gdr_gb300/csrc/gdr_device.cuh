@@ -107,6 +107,16 @@ __device__ __forceinline__ void store_f32(float *p, long long stride, bool vec, 
     for (int i = 0; i < N; ++i) p[i * stride] = x[i];
 }
 
+// Zeroes C output columns of n consecutive tokens starting at row pointer o
+// (rows p.out_ss apart): the output of a skipped (row, head).
+template <int C>
+__device__ __forceinline__ void zero_rows(float *o, int n, const StepParams &p) {
+    float z[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) z[c] = 0.0f;
+    for (int t = 0; t < n; ++t) store_f32<C>(o + (long long)t * p.out_ss, p.out_vs, p.out_vec, z);
+}
+
 // ---- ring records: float32, or bfloat16 rounded to nearest-even once --------
 // i is an element index into the ring; i2 is even, i4 a multiple of 4 (the
 // ring base is 16-byte aligned and record strides keep the alignment).

@@ -26,7 +26,7 @@ namespace gdr {
 // caller's row-length bound); per-element beta (BPV) stages beta per token
 // like v and uses at most 8 tokens.
 template <typename ST, int K, int VV = K, bool BPV = false, int TCX = 16> struct ChainShape {
-    static constexpr int V = VV;                   // value head size: K or 2K
+    static constexpr int V = VV;                   // value head size: K, 2K or K/2
     static constexpr int NG = K / 8;               // row groups
     // lanes along K: 4 (32 rows per lane at K = 128), or 2 for K = 128 with
     // 32-token chunks or a float32 state.  Long rows run one CTA per row and
@@ -132,22 +132,18 @@ __global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX>::NT,
     }
     const int L = t1 - t0;
     if (L == 0 && !p.dense) return;  // the dense mode still hands the start state on
-    if (max_len > 0 && L > max_len) {
-        if (leader) flag(p.status, GDR_STATUS_ROW_TOO_LONG);
-        return;
-    }
     const int wcol = warp * WC + vl * C;           // lane's first column inside the slice
     const int col0 = slice * VS + wcol;            // ... inside the head
     float *obase = p.out + (long long)t0 * p.out_ss + (long long)(h * V + col0) * p.out_vs;
+    if (max_len > 0 && L > max_len) {  // longer than the caller's bound: zero output, nothing else
+        if (leader) flag(p.status, GDR_STATUS_ROW_TOO_LONG);
+        if (kl == 0) zero_rows<C>(obase, L, p);
+        return;
+    }
     const int slot = p.dense ? b : p.slot_idx[b];
     if (slot < 0 || slot >= p.max_slots) {
         if (slot != -1 && leader) flag(p.status, GDR_STATUS_BAD_SLOT);
-        if (kl == 0) {
-            float z[C];
-#pragma unroll
-            for (int c = 0; c < C; ++c) z[c] = 0.0f;
-            for (int t = 0; t < L; ++t) store_f32<C>(obase + (long long)t * p.out_ss, p.out_vs, p.out_vec, z);
-        }
+        if (kl == 0) zero_rows<C>(obase, L, p);
         return;
     }
 
@@ -356,8 +352,9 @@ constexpr int kChainLongTC = 32;
 constexpr int kChainOrderRows = 32;
 
 // The launchers of each pass (one translation unit each, so they compile in
-// parallel).
+// parallel; the forward pass with V != K has its own).
 cudaError_t launch_chain_fwd(const StepParams &p, int K, int V, bool bf16, long long max_len, cudaStream_t st);
+cudaError_t launch_chain_fwd_kv(const StepParams &p, int K, int V, bool bf16, long long max_len, cudaStream_t st);
 cudaError_t launch_chain_verify(const StepParams &p, int K, bool bf16, const RingParams &rp, long long max_len,
                                 cudaStream_t st);
 cudaError_t launch_chain_snap(const StepParams &p, int K, int V, bool bf16, const SnapParams &sp, long long max_len,
@@ -383,6 +380,21 @@ inline cudaError_t launch_chain_k(const StepParams &p, const RingParams &rp, con
     const int order_p = (p.batch <= Sh::NT && p.batch <= kChainOrderRows && blocks > li.sms) ? li.sms : 0;
     k_chain<ST, K, V, MODE, BPV, TCX><<<(unsigned)blocks, Sh::NT, Sh::SMEM, st>>>(p, rp, sp, max_len, order_p);
     return cudaGetLastError();
+}
+
+// The forward pass of one (state type, K, V): the chunk size follows the
+// caller's row-length bound -- rows bounded at 8 or 16 tokens get chunks of
+// that size (a smaller stage, more L1); longer or unbounded rows take
+// kChainLongTC (fewer chunk barriers and normalisation passes per token).
+template <typename ST, int K, int V>
+inline cudaError_t launch_chain_fwd_t(const StepParams &p, long long max_len, cudaStream_t st) {
+    const RingParams rp{};
+    const SnapParams sp{};
+    if (p.bpv) return launch_chain_k<ST, K, V, Mode::Fwd, true, 8>(p, rp, sp, max_len, st);
+    if (max_len >= 1 && max_len <= 8) return launch_chain_k<ST, K, V, Mode::Fwd, false, 8>(p, rp, sp, max_len, st);
+    if (max_len >= 1 && max_len <= 16)
+        return launch_chain_k<ST, K, V, Mode::Fwd, false, 16>(p, rp, sp, max_len, st);
+    return launch_chain_k<ST, K, V, Mode::Fwd, false, kChainLongTC>(p, rp, sp, max_len, st);
 }
 
 }  // namespace gdr

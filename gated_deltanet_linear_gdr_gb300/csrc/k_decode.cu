@@ -46,21 +46,17 @@ __global__ void __launch_bounds__(kDecodeThreads) k_decode(const StepParams p) {
         return;
     }
     if (t1 == t0) return;
-    if (t1 - t0 > 1) {
-        if (leader) flag(p.status, GDR_STATUS_ROW_TOO_LONG);
-        return;
-    }
     const int col0 = slice * WC + vl * C;
     float *orow = p.out + (long long)t0 * p.out_ss + (long long)(h * V + col0) * p.out_vs;
+    if (t1 - t0 > 1) {  // longer than the caller's bound: zero output, nothing else
+        if (leader) flag(p.status, GDR_STATUS_ROW_TOO_LONG);
+        if (kl == 0) zero_rows<C>(orow, t1 - t0, p);
+        return;
+    }
     const int slot = p.slot_idx[b];
     if (slot < 0 || slot >= p.max_slots) {
         if (slot != -1 && leader) flag(p.status, GDR_STATUS_BAD_SLOT);
-        if (kl == 0) {
-            float z[C];
-#pragma unroll
-            for (int c = 0; c < C; ++c) z[c] = 0.0f;
-            store_f32<C>(orow, p.out_vs, p.out_vec, z);
-        }
+        if (kl == 0) zero_rows<C>(orow, 1, p);
         return;
     }
 
@@ -195,20 +191,16 @@ __device__ __forceinline__ void unit_compute(const StepParams &p, const UnitMeta
         return;
     }
     if (m.t1 == m.t0) return;
-    if (m.t1 - m.t0 > 1) {
-        if (leader) flag(p.status, GDR_STATUS_ROW_TOO_LONG);
-        return;
-    }
     const int col = warp * Sh::WC + vl * C;  // inside the unit's tile
     float *orow = p.out + (long long)m.t0 * p.out_ss + (long long)(h * V + us * Sh::CW + col) * p.out_vs;
+    if (m.t1 - m.t0 > 1) {  // longer than the caller's bound: zero output, nothing else
+        if (leader) flag(p.status, GDR_STATUS_ROW_TOO_LONG);
+        if (kl == 0) zero_rows<C>(orow, m.t1 - m.t0, p);
+        return;
+    }
     if (m.slot < 0 || m.slot >= p.max_slots) {
         if (m.slot != -1 && leader) flag(p.status, GDR_STATUS_BAD_SLOT);
-        if (kl == 0) {
-            float z[C];
-#pragma unroll
-            for (int c = 0; c < C; ++c) z[c] = 0.0f;
-            store_f32<C>(orow, p.out_vs, p.out_vec, z);
-        }
+        if (kl == 0) zero_rows<C>(orow, 1, p);
         return;
     }
     const float *qs = reinterpret_cast<const float *>(stage + Sh::S_STATE);

@@ -414,13 +414,19 @@ cudaError_t launch_fold(const FoldParams &p, int K, bool bf16, cudaStream_t s) {
     return cudaErrorInvalidValue;
 }
 
+// V = K, V = 2K, and V = K/2 for K >= 32.
+template <typename ST, int K> static cudaError_t rollback_v(const RollbackParams &p, int V, cudaStream_t s) {
+    if (V == K) return launch_rollback_t<ST, K, K>(p, s);
+    if (V == 2 * K) return launch_rollback_t<ST, K, 2 * K>(p, s);
+    if constexpr (K >= 32) {
+        if (2 * V == K) return launch_rollback_t<ST, K, K / 2>(p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_rollback(const RollbackParams &p, int K, int V, bool bf16, cudaStream_t s) {
-#define GDR_CASE(KK)                                                                                      \
-    case KK:                                                                                              \
-        if (V == KK) return bf16 ? launch_rollback_t<uint16_t, KK, KK>(p, s) : launch_rollback_t<float, KK, KK>(p, s); \
-        if (V == 2 * KK)                                                                                  \
-            return bf16 ? launch_rollback_t<uint16_t, KK, 2 * KK>(p, s) : launch_rollback_t<float, KK, 2 * KK>(p, s); \
-        return cudaErrorInvalidValue;
+#define GDR_CASE(KK) \
+    case KK: return bf16 ? rollback_v<uint16_t, KK>(p, V, s) : rollback_v<float, KK>(p, V, s);
     switch (K) {
         GDR_CASE(16)
         GDR_CASE(32)

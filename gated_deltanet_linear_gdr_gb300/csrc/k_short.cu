@@ -217,20 +217,16 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
     }
     const int L = m.t1 - m.t0;
     if (L == 0) return false;
-    if (max_len > 0 && L > max_len) {
-        if (leader) flag(p.status, GDR_STATUS_ROW_TOO_LONG);
-        return false;
-    }
     const int col = warp * W::WC + vl * C;  // inside the unit's tile
     float *optr = p.out + (long long)m.t0 * p.out_ss + (long long)(h * V + us * P::CW + col) * p.out_vs;
+    if (max_len > 0 && L > max_len) {  // longer than the caller's bound: zero output, nothing else
+        if (leader) flag(p.status, GDR_STATUS_ROW_TOO_LONG);
+        if (kl == 0) zero_rows<C>(optr, L, p);
+        return false;
+    }
     if (m.slot < 0 || m.slot >= p.max_slots) {
         if (m.slot != -1 && leader) flag(p.status, GDR_STATUS_BAD_SLOT);
-        if (kl == 0) {
-            float z[C];
-#pragma unroll
-            for (int c = 0; c < C; ++c) z[c] = 0.0f;
-            for (int t = 0; t < L; ++t) store_f32<C>(optr + (long long)t * p.out_ss, p.out_vs, p.out_vec, z);
-        }
+        if (kl == 0) zero_rows<C>(optr, L, p);
         return false;
     }
     // Verify: rows of at most ring_len tokens record and leave the pool alone.

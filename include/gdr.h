@@ -40,10 +40,11 @@
  *     library picks: every pass uses one fixed order of float32 operations per
  *     (row, head), so the same row gives the same bits in any call.
  *   - Two live rows of one call must not share a pool slot (they would race).
- *   - Head sizes: K in {16, 32, 64, 128}; V = K, or V = 2K for the forward,
- *     dense and snapshot passes and rollback ("core.ssm.ops.gdp.fused_recurrent"
- *     sizes K and V separately; the verify ring and fold need V = K, as
- *     "gated_delta_recurrence_verify_ring_gpu" requires).
+ *   - Head sizes: K in {16, 32, 64, 128}; V = K, or V = 2K or (for K >= 32)
+ *     V = K/2 for the forward, dense and snapshot passes and rollback
+ *     ("core.ssm.ops.gdp.fused_recurrent" sizes K and V separately); the verify
+ *     ring and fold need V = K, as "gated_delta_recurrence_verify_ring_gpu"
+ *     requires.
  */
 #ifndef GDR_H
 #define GDR_H
@@ -279,8 +280,11 @@ int gdr_fold(const gdr_step_args *args, const void *ring, int32_t ring_dtype,
  * state after step (i+1)*steps_per_token - 1 of a row is stored at
  *     inter[slot, i, h, :, :]  = inter + slot*inter_slot_stride +
  *                               i*inter_token_stride + h*inter_head_stride
- * (a dense [K, V] block in the pool's dtype) for every i < n_inter.  A partial
- * trailing draft is not stored; padding rows store nothing.  A row with more
+ * (a dense [K, V] block in the pool's dtype) for every i < n_inter.  inter is
+ * indexed by pool slot: it must hold a block row for every slot in
+ * [0, max_slots) (a slot the device accepts as valid is never checked against
+ * a smaller buffer).  A partial trailing draft is not stored; padding rows
+ * store nothing.  A row with more
  * complete drafts than n_inter stores the first n_inter and sets
  * GDR_STATUS_SNAPSHOT_OVERFLOW.  Strides must keep 16-byte alignment. */
 int gdr_fwd_snapshots(const gdr_step_args *args, void *inter, int64_t inter_slot_stride,
@@ -290,7 +294,8 @@ int gdr_fwd_snapshots(const gdr_step_args *args, void *inter, int64_t inter_slot
 /* Rollback ("core.ssm.ops.gdp.fused_recurrent", intermediate_states: roll the
  * recurrence back to any accepted prefix): state[slot_idx[b], h] <-
  * inter[slot_idx[b], accepted[b], h] for every value head.  accepted[b] == -1
- * or slot -1 skips the row.  Uses from `args`: batch, nv, K, V, state*,
+ * or slot -1 skips the row.  As for gdr_fwd_snapshots, inter must hold a block
+ * row for every slot in [0, max_slots).  Uses from `args`: batch, nv, K, V, state*,
  * max_slots, slot_idx. */
 int gdr_rollback(const gdr_step_args *args, const void *inter, int64_t inter_slot_stride,
                  int64_t inter_token_stride, int64_t inter_head_stride, int32_t n_inter,

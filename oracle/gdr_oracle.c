@@ -35,7 +35,7 @@
  *     S  = S + k^ u^T                                (rank-one update)
  *     o  = scale * S^T q^                            (readout of the new state)
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - order decay -> correction -> update -> readout (readout of the updated
  *     state), matching S_t = alpha (I - beta k k^T) S_{t-1} + beta k v^T;
  *   - value head h reads key head h / (nv/nk) (contiguous GQA groups);

@@ -50,13 +50,13 @@ class Dev:
         return gdr.gdr_fwd(self.qkv, self.decay, self.beta, self.state, self.slot, self.off,
                            out=out, max_row_len=max_row_len, **self.kw)
 
-    def verify(self, ring, ring_slot, max_row_len=0):
+    def verify(self, ring, ring_slot, max_row_len=0, out=None):
         return gdr.gdr_verify_ring(self.qkv, self.decay, self.beta, self.state, self.slot,
-                                   self.off, ring, ring_slot, max_row_len=max_row_len, **self.kw)
+                                   self.off, ring, ring_slot, out=out, max_row_len=max_row_len, **self.kw)
 
-    def snapshots(self, inter, spt, max_row_len=0):
+    def snapshots(self, inter, spt, max_row_len=0, out=None):
         return gdr.gdr_fwd_snapshots(self.qkv, self.decay, self.beta, self.state, self.slot,
-                                     self.off, inter, spt, max_row_len=max_row_len, **self.kw)
+                                     self.off, inter, spt, out=out, max_row_len=max_row_len, **self.kw)
 
 
 def check_out(gpu_out: torch.Tensor, ref: np.ndarray, atol=OUT_ATOL):

@@ -98,7 +98,8 @@ def _valid_args():
 
 
 BAD = [
-    ("V not K or 2K", lambda a: setattr(a, "V", 48), B.GDR_ERR_UNSUPPORTED),
+    ("V not K, 2K or K/2", lambda a: setattr(a, "V", 48), B.GDR_ERR_UNSUPPORTED),
+    ("V = K/2 at K = 16", lambda a: setattr(a, "V", 8), B.GDR_ERR_UNSUPPORTED),
     ("K unsupported", lambda a: (setattr(a, "K", 48), setattr(a, "V", 48)), B.GDR_ERR_UNSUPPORTED),
     ("nv % nk", lambda a: setattr(a, "nk", 3), B.GDR_ERR_INVALID_ARG),
     ("nv <= 0", lambda a: setattr(a, "nv", 0), B.GDR_ERR_INVALID_ARG),
@@ -180,6 +181,12 @@ def test_verify_and_fold_need_v_equal_k(lib):
         B.GDR_ERR_UNSUPPORTED
     assert lib.gdr_fold(ctypes.byref(a), fake, B.GDR_F32, 4, 8, need, fake, fake, None) == \
         B.GDR_ERR_UNSUPPORTED
+    a.K, a.V = 64, 32  # K/2: also forward-only
+    need = lib.gdr_ring_record_elements(64, 32, 2)
+    assert lib.gdr_verify_ring(ctypes.byref(a), fake, B.GDR_F32, 4, 8, need, fake, None) == \
+        B.GDR_ERR_UNSUPPORTED
+    assert lib.gdr_fold(ctypes.byref(a), fake, B.GDR_F32, 4, 8, need, fake, fake, None) == \
+        B.GDR_ERR_UNSUPPORTED
 
 
 def test_fwd_dense_rejects_bad_buffers(lib):
@@ -224,6 +231,16 @@ def test_snapshots_and_rollback_reject_bad_buffers(lib):
         B.GDR_ERR_INVALID_ARG
     assert lib.gdr_rollback(ctypes.byref(a), fake, 4 * 4 * hs, 4 * hs + 1, hs, 4, fake, None) == \
         B.GDR_ERR_UNSUPPORTED
+
+
+def test_binding_rejects_short_intermediate_buffer():
+    """The kernels index intermediate_states by pool slot, so the binding refuses
+    a buffer with fewer slot rows than the pool (host-side check, no GPU)."""
+    import torch
+    state = torch.zeros((6, 2, 16, 16))
+    with pytest.raises(ValueError, match="slot rows"):
+        B._inter_strides(torch.zeros((5, 3, 2, 16, 16)), state)
+    assert B._inter_strides(torch.zeros((6, 3, 2, 16, 16)), state)[3] == 3
 
 
 def test_empty_batch_is_a_no_op(lib):

@@ -135,6 +135,23 @@ def test_value_head_twice_key_head_equals_two_halves(state_dtype):
 
 
 @pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
+def test_key_head_twice_value_head_equals_half_of_a_square_pass(state_dtype):
+    """A V = K/2 pass is, bit for bit, the first half of the value columns of a
+    V = K pass whose other columns hold anything: columns never mix."""
+    K = 128
+    for hint, lengths in ((0, [19, 2, 1, 40]), (16, [16, 2, 1, 9]), (8, [8, 2, 0, 5])):
+        w = W.random_case(821 + hint, lengths, nk=2, nv=4, K=K, max_slots=6, state_dtype=state_dtype)
+        pool = w.state_pool()
+        out, after = _run_fwd(w, pool, max_row_len=hint)
+        nv, qk, H = w.nv, 2 * w.nk * K, K // 2
+        v = w.qkv[:, qk:].reshape(-1, nv, K)[:, :, :H].reshape(-1, nv * H)
+        wh = dataclasses.replace(w, V=H, qkv=np.ascontiguousarray(np.concatenate([w.qkv[:, :qk], v], axis=1)))
+        out_h, after_h = _run_fwd(wh, np.ascontiguousarray(pool[..., :H]), max_row_len=hint)
+        assert (out.reshape(-1, nv, K)[:, :, :H].view(np.uint32) == out_h.reshape(-1, nv, H).view(np.uint32)).all()
+        assert (after[..., :H] == after_h).all()
+
+
+@pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
 def test_dense_state_equals_pool_at_the_rows_slots(state_dtype):
     """The dense mode is the slot-indexed pass with the rows' states gathered:
     same output bits, final[b] = the pool slot of row b after the pass; also
@@ -378,10 +395,62 @@ def test_device_status_flags_bad_inputs():
     assert (out[2:3] == 0).all()                     # the bad row's output is zeroed
     assert (pool_to_host(d.state)[[1, 3]] == pool[[1, 3]]).all()
     d = Dev(w, pool)
-    d.fwd(max_row_len=2)                              # a row of 3 tokens breaks the bound
+    out = torch.full((w.total_tokens, w.nv * w.V), float("nan"), device=DEV)
+    d.fwd(max_row_len=2, out=out)                     # a row of 3 tokens breaks the bound
     st = gdr.gdr_get_status(clear=True)
     assert st & 0x10, gdr.status_names(st)
+    assert (out[3:6] == 0).all()                     # ... and its output is zeroed
     assert gdr.gdr_get_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("K,state_dtype", [(16, "f32"), (128, "bf16"), (128, "f32")])
+def test_row_longer_than_bound_zeroes_its_output(K, state_dtype):
+    """A row longer than the caller's max_row_len is skipped by the forward,
+    verify and snapshot passes (short-row kernel at K = 128, general kernel at
+    K = 16): its output rows are zeroed, its slot, ring row and snapshots are
+    left alone, ROW_TOO_LONG is flagged, and the other rows keep the bits of
+    an unbounded call."""
+    w = W.random_case(607, [2, 1, 3], nk=1, nv=2, K=K, max_slots=4, state_dtype=state_dtype)
+    pool = w.state_pool()
+    o_ref, s_ref = _run_fwd(w, pool)
+    s2 = int(w.slot_idx[2])
+
+    def nan_out():
+        return torch.full((w.total_tokens, w.nv * w.V), float("nan"), device=DEV)
+
+    def check(out):
+        st = gdr.gdr_get_status(clear=True)
+        assert st == 0x10, gdr.status_names(st)
+        o = out.cpu().numpy()
+        assert (o[3:6] == 0).all()
+        assert (o[:3].view(np.uint32) == o_ref[:3].view(np.uint32)).all()
+
+    d = Dev(w, pool)
+    out = nan_out()
+    d.fwd(max_row_len=2, out=out)
+    check(out)
+    host = pool_to_host(d.state)
+    assert (host[s2] == pool[s2]).all()
+    for b in (0, 1):
+        s = int(w.slot_idx[b])
+        assert (host[s] == s_ref[s]).all()
+
+    d = Dev(w, pool)
+    out = nan_out()
+    ring = ring_for(w, 4, 3)
+    d.verify(ring, torch.arange(3, dtype=torch.int32, device=DEV), max_row_len=2, out=out)
+    check(out)
+    assert torch.isnan(ring[2]).all()
+    assert (pool_to_host(d.state) == pool).all()
+
+    d = Dev(w, pool)
+    out = nan_out()
+    tdt = torch.bfloat16 if state_dtype == "bf16" else torch.float32
+    inter = torch.full((w.max_slots, 3, w.nv, w.K, w.V), float("nan"), dtype=tdt, device=DEV)
+    d.snapshots(inter, 1, max_row_len=2, out=out)
+    check(out)
+    assert torch.isnan(inter[s2].float()).all()
+    assert (pool_to_host(d.state)[s2] == pool[s2]).all()
 
 
 @pytest.mark.parametrize("state_dtype", ["bf16", "f32"])
@@ -421,9 +490,12 @@ def test_decode_kernel_device_checks():
     offs = np.concatenate([[0], np.arange(2, w.batch + 1)]).astype(np.int32)  # row 0 has 2 tokens
     two = dataclasses.replace(w, offsets=offs, slot_idx=w.slot_idx[:-1].copy())
     d = Dev(two, pool)
-    d.fwd(max_row_len=1)
+    out = torch.full((w.total_tokens, w.nv * w.V), float("nan"), device=DEV)
+    d.fwd(max_row_len=1, out=out)
     st = gdr.gdr_get_status(clear=True)
     assert st & 0x10, gdr.status_names(st)
+    assert (out[0:2] == 0).all()  # the skipped row's two tokens
+    assert not torch.isnan(out).any()
     s0 = int(two.slot_idx[0])
     if s0 >= 0:
         assert (pool_to_host(d.state)[s0] == pool[s0]).all()

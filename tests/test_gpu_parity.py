@@ -100,14 +100,18 @@ def test_decode_config_through_general_kernel():
 
 def test_prefill_config_sampled_rows():
     """The ragged prefill workload at full size on the GPU; the oracle recomputes
-    the two shortest rows (rows are independent)."""
+    the two shortest rows, a middle one and the longest (3514 tokens at this
+    seed: the row where float32 rounding has the longest run to build up and
+    the bf16 state must still land within one ulp).  Rows are independent."""
     w = W.prefill()
     pool = w.state_pool()
     d = Dev(w, pool)
     out = d.fwd()
     torch.cuda.synchronize()
     L = w.row_lengths
-    rows = list(np.argsort(L)[:2])
+    order = np.argsort(L, kind="stable")
+    rows = sorted({int(order[0]), int(order[1]), int(order[len(order) // 2]), int(order[-1])})
+    assert L[rows].max() == L.max()
     sub = sub_workload(w, rows)
     p = problem(sub, state=pool.copy())
     ref = oracle.fwd(p)
@@ -191,9 +195,30 @@ def test_value_head_twice_key_head_forward(K, state_dtype, hint):
     _fwd_parity(w, max_row_len=hint)
 
 
+@pytest.mark.parametrize("K", [32, 64, 128])
 @pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
-def test_value_head_twice_key_head_snapshots_rollback_dense(state_dtype):
-    w = W.random_case(810, [8, 6, 8], nk=2, nv=4, K=64, V=128, max_slots=6, state_dtype=state_dtype,
+@pytest.mark.parametrize("hint", [0, 1, 16])  # the general kernel's 32-, 8- and 16-token chunks
+def test_key_head_twice_value_head_forward(K, state_dtype, hint):
+    """V = K/2 ("core.ssm.ops.gdp.fused_recurrent": q, k [B, T, H, K] and v
+    [B, T, HV, V] sized separately) against the oracle: ragged rows, an empty
+    row and a padding row."""
+    lengths = [1, 18, 0, 7, 40] if hint == 0 else [1, 1, 1, 0] if hint == 1 else [16, 3, 0, 9]
+    w = W.random_case(830 + K + hint, lengths, nk=2, nv=4, K=K, V=K // 2, max_slots=9,
+                      state_dtype=state_dtype, n_pad=1)
+    _fwd_parity(w, max_row_len=hint)
+
+
+@pytest.mark.parametrize("K", [32, 128])
+def test_key_head_twice_value_head_beta_per_value(K):
+    w = W.random_case(850 + K, [5, 12, 1], nk=1, nv=2, K=K, V=K // 2, max_slots=4, state_dtype="bf16",
+                      beta_per_value=True)
+    _fwd_parity(w)
+
+
+@pytest.mark.parametrize("V", [128, 32])  # 2K and K/2
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_value_head_twice_key_head_snapshots_rollback_dense(state_dtype, V):
+    w = W.random_case(810, [8, 6, 8], nk=2, nv=4, K=64, V=V, max_slots=6, state_dtype=state_dtype,
                       decay_is_log=True)
     pool = w.state_pool()
     d = Dev(w, pool)
@@ -332,7 +357,7 @@ def test_gdp_snapshot_config_and_rollback(hint):
     inter = torch.full((w.max_slots, w.n_inter, w.nv, w.K, w.V), float("nan"), device=DEV)
     out = d.snapshots(inter, w.steps_per_token, max_row_len=hint)
     torch.cuda.synchronize()
-    sub_rows = [0, 1, 2]  # oracle on a sample of requests
+    sub_rows = list(range(w.batch))  # the oracle over every request
     sub = sub_workload(w, sub_rows)
     p = problem(sub, state=pool.copy())
     oint = np.full((w.max_slots, w.n_inter, w.nv, w.K, w.V), np.nan, np.float32)

@@ -76,6 +76,8 @@ def _load():
                 getattr(lib, f"oracle_fwd_snapshots_{prec}").argtypes = [P, vp, vp, i32, i32]
                 getattr(lib, f"oracle_fold_{prec}").argtypes = [P, vp, i32, i32, i32, i32, vp, vp]
             lib.oracle_rollback.argtypes = [P, vp, i32, vp]
+            i64 = ctypes.c_int64
+            lib.oracle_conv1d.argtypes = [i32, i64, i32, i32, vp, vp, vp, i32, vp, i64, vp, vp, vp]
             lib.oracle_round_bf16.argtypes = [ctypes.c_double]
             lib.oracle_round_bf16.restype = ctypes.c_uint16
             lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -219,6 +221,44 @@ def rollback(p: Problem, inter: np.ndarray, accepted) -> None:
     s = p._c_struct()
     _check(lib.oracle_rollback(ctypes.byref(s), _ptr(inter), inter.shape[1], _ptr(acc)),
            "rollback")
+
+
+def conv1d(x, weight, bias, silu: bool, conv_state, slot_idx, offsets) -> np.ndarray:
+    """Pass-1 causal depthwise convolution ("gated_delta_recurrence_fwd_gpu",
+    Args: qkv_conv_output is its output): x [T, C] float32, weight [C, W],
+    bias [C] or None, SiLU or none; conv_state [slots, C, W-1] float32 is read
+    at slot_idx and updated in place (None when W == 1).  Returns the float32
+    output [T, C] (the readings are listed in gdr_oracle.c)."""
+    lib = _load()
+    x = _c(x, np.float32)
+    weight = _c(weight, np.float32)
+    C, Wd = weight.shape
+    T = x.shape[0]
+    assert x.shape == (T, C)
+    b = None if bias is None else _c(bias, np.float32)
+    if conv_state is not None:
+        assert conv_state.dtype == np.float32 and conv_state.flags.c_contiguous
+        assert conv_state.shape[1:] == (C, Wd - 1)
+        slots = conv_state.shape[0]
+    else:
+        assert Wd == 1
+        slots = 1 << 30
+    si = _c(slot_idx, np.int32)
+    off = _c(offsets, np.int32)
+    y = np.zeros((T, C), np.float32)
+    _check(lib.oracle_conv1d(si.shape[0], T, C, Wd, _ptr(x), _ptr(weight), _ptr(b), int(bool(silu)),
+                             _ptr(conv_state), slots, _ptr(si), _ptr(off), _ptr(y)), "conv1d")
+    return y
+
+
+def fwd_conv(p: Problem, weight, bias, silu: bool, conv_state, work: str = "f64") -> np.ndarray:
+    """The forward pass on Pass-1 output: p.qkv holds the RAW convolution input;
+    the convolution (conv1d, conv_state updated in place) produces
+    qkv_conv_output, which the recurrence then reads.  Returns out [T, nv*V]."""
+    y = conv1d(p.qkv, weight, bias, silu, conv_state, p.slot_idx, p.offsets)
+    q = Problem(y, p.decay, p.beta, p.state, p.slot_idx, p.offsets, nk=p.nk, nv=p.nv, K=p.K, V=p.V,
+                decay_is_log=p.decay_is_log, use_l2norm=p.use_l2norm, scale=p.scale, eps=p.eps)
+    return fwd(q, work)
 
 
 def round_bf16(x) -> np.ndarray:

@@ -173,6 +173,76 @@ static int check_problem(const oracle_problem *p)
 #undef SQRT
 #undef EXP
 
+/* ---- Pass-1 causal depthwise convolution ------------------------------- */
+
+/* "gated_delta_recurrence_fwd_gpu", Args: qkv_conv_output is the "Conv1d
+ * output from Pass 1".  The pages give only that output's layout; the
+ * convolution is taken as the plain causal depthwise one over the conv_dim
+ * channels, with every parameter from the caller (readings, each a choice the
+ * pages leave open):
+ *   - each channel c has its own `width` taps w[c][0..width-1]; for token j of
+ *     a row, with xe = (the slot's conv state for c, oldest first) followed by
+ *     the row's inputs x[t0 .. t1-1][c],
+ *         y[t0+j][c] = bias[c] + sum_m w[c][m] * xe[j + m]
+ *     so tap width-1 multiplies the newest input x[t0+j][c];
+ *   - bias is optional (none: 0); the activation is none or SiLU,
+ *     y / (1 + exp(-y));
+ *   - the conv state pool [max_slots, channels, width-1] (float32) is read at
+ *     slot_idx[b] and replaced by the last width-1 entries of xe (a row
+ *     shorter than width-1 keeps part of the old state);
+ *   - a padding row (slot -1) or an empty row leaves the slot alone; its
+ *     output rows are set to 0;
+ *   - the output is float32, the layout of qkv_conv_output.
+ * Computed in double, rounded to float once. */
+int oracle_conv1d(int32_t batch, int64_t total_tokens, int32_t channels, int32_t width,
+                  const float *x, const float *weight, const float *bias, int32_t silu,
+                  float *conv_state, int64_t max_slots, const int32_t *slot_idx,
+                  const int32_t *offsets, float *y)
+{
+    if (batch < 0 || total_tokens < 0 || channels <= 0 || width < 1 || !weight || !slot_idx ||
+        !offsets || !y || (total_tokens > 0 && !x) || (width > 1 && !conv_state && batch > 0))
+        return -1;
+    const int w1 = width - 1;
+    double *xe = (double *)malloc(sizeof(double) * (size_t)(w1 + total_tokens + 1));
+    if (!xe)
+        return -1;
+    for (int b = 0; b < batch; ++b) {
+        const int t0 = offsets[b], t1 = offsets[b + 1], slot = slot_idx[b];
+        if (t0 < 0 || t1 < t0 || t1 > total_tokens || slot < -1 || slot >= max_slots) {
+            free(xe);
+            return -1;
+        }
+        const int L = t1 - t0;
+        if (slot < 0) {
+            for (int t = t0; t < t1; ++t)
+                for (int c = 0; c < channels; ++c)
+                    y[(size_t)t * channels + c] = 0.0f;
+            continue;
+        }
+        if (L == 0)
+            continue;
+        for (int c = 0; c < channels; ++c) {
+            float *st = conv_state ? conv_state + ((size_t)slot * channels + c) * w1 : NULL;
+            for (int i = 0; i < w1; ++i)
+                xe[i] = st[i];
+            for (int j = 0; j < L; ++j)
+                xe[w1 + j] = x[(size_t)(t0 + j) * channels + c];
+            for (int j = 0; j < L; ++j) {
+                double acc = bias ? (double)bias[c] : 0.0;
+                for (int m = 0; m < width; ++m)
+                    acc += (double)weight[(size_t)c * width + m] * xe[j + m];
+                if (silu)
+                    acc = acc / (1.0 + exp(-acc));
+                y[(size_t)(t0 + j) * channels + c] = (float)acc;
+            }
+            for (int i = 0; i < w1; ++i)
+                st[i] = (float)xe[L + i];
+        }
+    }
+    free(xe);
+    return 0;
+}
+
 /* ---- rollback: a plain copy, the same in both precisions --------------- */
 
 /* state[slot, h] <- intermediate[slot, accepted[b], h] for every value head.

@@ -48,13 +48,17 @@ def parse():
     ap.add_argument("--impl", default="gdr", choices=["gdr", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "prefill_dense", "prefill_v2k", "verify_fold", "verify_fold_bf16_ring",
+    ap.add_argument("--only", choices=["prefill", "prefill_dense", "prefill_v2k", "prefill_conv", "verify_fold",
+                                       "verify_fold_bf16_ring",
                                        "gdp_snapshots",
                                        "gdp_snapshots_beta_per_value"],
                     default=None,
                     help="time just this secondary workload and print its figures (profiling aid)")
     ap.add_argument("--soak-s", type=float, default=1.0,
                     help="seconds of untimed steps after warm-up (steady clocks)")
+    ap.add_argument("--copy-bandwidth", action="store_true",
+                    help="print the pinned host<->device copy bandwidth against copy size and exit "
+                         "(the link the end-to-end figure runs over)")
     return ap.parse_args()
 
 
@@ -289,6 +293,34 @@ def bench_prefill(dev, flush, stream, hbm_peak, steps, V=0):
     }
 
 
+def bench_prefill_conv(dev, flush, stream, hbm_peak, steps):
+    """The ragged prefill workload from the RAW Pass-1 input: the causal
+    depthwise convolution (width 4, SiLU, bias) fused into the recurrence's
+    operand staging, then the conv-state update (gdr_fwd_conv)."""
+    import torch
+    import gated_deltanet_linear_gdr_gb300 as gdr
+    from gated_deltanet_linear_gdr_gb300 import workloads as W
+    w = W.prefill()
+    cv = W.conv_inputs(w, width=4, seed=2)
+    st = _pool_dev(w, dev)
+    x, dec, bet, slot, off = (_to_dev(a, dev) for a in (w.qkv, w.decay, w.beta, w.slot_idx, w.offsets))
+    wt, bs, cs = (_to_dev(a, dev) for a in (cv.weight, cv.bias, cv.state))
+    out = torch.empty((w.total_tokens, w.nv * w.V), device=dev)
+    fn = gdr.prepare_fwd_conv(x, dec, bet, st, slot, off, wt, bs, cs, out)
+    for _ in range(2):
+        fn()
+    ms = statistics.median(time_steps(fn, max(3, steps // 10), flush, stream))
+    ht = w.live_head_tokens
+    fp32_peak = fp32_fma_peak(dev)
+    return {
+        "workload": f"ragged prefill from the raw Pass-1 input: {w.batch} rows, T={w.total_tokens}, nk=16, nv=32, "
+                    "K=V=128, bf16 pool [16,32,128,128], conv width 4 + bias + SiLU fused, conv state "
+                    "[16,8192,3] fp32",
+        "ms": ms, "head_tokens_per_s": ht / (ms * 1e-3),
+        "frac_fp32_fma": fma_ops(ht, w.K, w.V) / (ms * 1e-3) / fp32_peak,
+    }
+
+
 def bench_prefill_v2k(dev, flush, stream, hbm_peak, steps):
     """The ragged prefill workload with value heads twice the key heads (V = 256)."""
     return bench_prefill(dev, flush, stream, hbm_peak, steps, V=256)
@@ -428,6 +460,7 @@ def bench_gdp_snapshots_beta_per_value(dev, flush, stream, hbm_peak, steps):
 
 
 SECONDARY = {"prefill": bench_prefill, "prefill_dense": bench_prefill_dense, "prefill_v2k": bench_prefill_v2k,
+             "prefill_conv": bench_prefill_conv,
              "verify_fold": bench_verify_fold,
              "verify_fold_bf16_ring": bench_verify_fold_bf16_ring,
              "gdp_snapshots": bench_gdp_snapshots,
@@ -445,22 +478,164 @@ def secondary(dev, flush, stream, hbm_peak, steps, only=None):
     return res
 
 
-def cpu_baseline_decode(w, budget_s=10.0):
-    """The CPU oracle (float64 C loops, one thread) on whole decode batches."""
+# ---------------------------------------------------- CPU baseline (oracle) ---
+# The oracle (float64 C loops, test infrastructure) timed on the host's cores
+# as it stands: rows and key-head groups are independent, so a workload is cut
+# into independent pieces and the pieces are run on Python threads (the C
+# oracle runs with the GIL released).  Single-thread and all-core figures.
+
+def host_cpu():
+    """(logical CPUs, CPU model string) of the host the oracle runs on."""
+    n = os.cpu_count() or 1
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k.strip().lower() in ("model name", "cpu model", "hardware") and v.strip():
+                    model = v.strip()
+                    break
+    except OSError:
+        pass
+    if not model:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                k, _, v = line.partition(":")
+                if k.strip() in ("Model name", "Vendor ID") and v.strip():
+                    model = (model + " " + v.strip()).strip()
+        except (OSError, subprocess.SubprocessError):
+            pass
+    import platform
+    return n, f"{model or 'unknown'} ({platform.machine()})"
+
+
+def cpu_piece(w, rows, heads=None, t_max=None):
+    """An independent piece of workload w as oracle.Problem arguments: rows
+    `rows` (each cut to its first t_max tokens), key heads `heads` (all when
+    None) with their value heads, and a compact pool holding only those rows'
+    slots (padding rows keep slot -1)."""
+    import numpy as np
+    nk, K, V = w.nk, w.K, w.V
+    r = w.nv // nk
+    hks = list(range(nk)) if heads is None else list(heads)
+    vh = [hk * r + j for hk in hks for j in range(r)]
+    toks, offs, slots, states = [], [0], [], []
+    for i, b in enumerate(rows):
+        t0, t1 = int(w.offsets[b]), int(w.offsets[b + 1])
+        if t_max is not None:
+            t1 = min(t1, t0 + t_max)
+        toks.extend(range(t0, t1))
+        offs.append(offs[-1] + t1 - t0)
+        live = int(w.slot_idx[b]) >= 0
+        slots.append(i if live else -1)
+        states.append(w.state_slot(int(w.slot_idx[b]))[vh] if live else None)
+    dt = np.uint16 if w.state_dtype == "bf16" else np.float32
+    pool = np.zeros((len(rows), len(vh), K, V), dt)
+    for i, st in enumerate(states):
+        if st is not None:
+            pool[i] = st
+    toks = np.asarray(toks, dtype=np.int64)
+    cols = ([c for hk in hks for c in range(hk * K, (hk + 1) * K)]
+            + [nk * K + c for hk in hks for c in range(hk * K, (hk + 1) * K)]
+            + [2 * nk * K + h * V + j for h in vh for j in range(V)])
+    beta = w.beta[toks][:, vh] if w.beta.ndim == 2 else w.beta[toks][:, vh, :]
+    return dict(qkv=w.qkv[toks][:, cols], decay=w.decay[toks][:, vh], beta=beta, state=pool,
+                slot_idx=np.asarray(slots, np.int32), offsets=np.asarray(offs, np.int32),
+                nk=len(hks), nv=len(vh), K=K, V=V, decay_is_log=w.decay_is_log,
+                use_l2norm=w.use_l2norm, scale=w.scale, eps=w.eps)
+
+
+def _cpu_time(pieces, run_piece, threads):
+    """Wall seconds to run every piece once on `threads` threads."""
+    from concurrent.futures import ThreadPoolExecutor
+    t0 = time.perf_counter()
+    if threads <= 1:
+        for pc in pieces:
+            run_piece(pc)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(run_piece, pieces))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(kind, w, budget_s=4.0, t_max=None):
+    """The oracle on workload w (kind: "fwd", "verify_fold", "snapshots"):
+    head-tokens/s on one thread and on every host core.  The sample is the
+    whole workload, or each row's first t_max tokens."""
+    import numpy as np
     import oracle
-    pool = w.state_pool(w.live_slots())
-    reps, t_total = 0, 0.0
-    while t_total < budget_s and reps < 100:
-        p = oracle.Problem(w.qkv, w.decay, w.beta, pool.copy(), w.slot_idx, w.offsets,
-                           nk=w.nk, nv=w.nv, K=w.K, V=w.V)
-        t0 = time.perf_counter()
-        oracle.fwd(p)
-        t_total += time.perf_counter() - t0
-        reps += 1
-    return {"value": w.live_head_tokens * reps / t_total, "unit": UNIT, "cores": 1,
-            "kind": "oracle",
-            "sample": f"{reps} whole decode batches (256 rows, {w.live_head_tokens} live "
-                      f"head-tokens each), float64 C loops, single thread, {t_total:.1f} s"}
+    ncpu, model = host_cpu()
+    L = np.diff(w.offsets.astype(np.int64))
+    if t_max is not None:
+        L = np.minimum(L, t_max)
+    head_tokens = int(L[w.slot_idx >= 0].sum()) * w.nv
+    rows = list(range(w.batch))
+    # pieces: one row (with every head) for short rows, one (row, key head) for long ones
+    by_head = t_max is not None or w.total_tokens > 4 * w.batch
+    pieces = []
+    for b in rows:
+        for hk in (range(w.nk) if by_head else [None]):
+            pc = cpu_piece(w, [b], None if hk is None else [hk], t_max)
+            if w.counts is not None:
+                pc["counts"] = w.counts[[b]].astype(np.int32)
+            if w.accepted is not None:
+                pc["accepted"] = w.accepted[[b]].astype(np.int32)
+            pieces.append(pc)
+    r = w.nv // w.nk
+
+    def run_piece(pc):
+        args = {k: v for k, v in pc.items() if k not in ("counts", "accepted")}
+        args["state"] = args["state"].copy()
+        prob = oracle.Problem(**args)
+        if kind == "fwd":
+            oracle.fwd(prob)
+        elif kind == "verify_fold":
+            nb = len(args["slot_idx"])
+            rec = oracle.ring_record_elements(prob.K, prob.V, r)
+            ring = np.zeros((nb, prob.nk, w.ring_len, rec), np.float32)
+            rsi = np.arange(nb, dtype=np.int32)
+            oracle.verify_ring(prob, ring, rsi, w.ring_len)
+            oracle.fold(prob, ring, rsi, pc["counts"], w.ring_len)
+        else:
+            nb = prob.state.shape[0]
+            inter = np.zeros((nb, w.n_inter, prob.nv, prob.K, prob.V), prob.state.dtype)
+            oracle.fwd_snapshots(prob, inter, w.steps_per_token)
+            oracle.rollback(prob, inter, pc["accepted"])
+
+    res = {}
+    for threads in (1, ncpu):
+        rounds, secs = 0, 0.0
+        while secs < budget_s and rounds < 50:
+            secs += _cpu_time(pieces, run_piece, threads)
+            rounds += 1
+        res[threads] = (head_tokens * rounds / secs, rounds, secs)
+    all_v, all_r, all_s = res[ncpu]
+    one_v, one_r, one_s = res[1]
+    sample = (f"{'first ' + str(t_max) + ' tokens of each row' if t_max else 'the whole workload'} "
+              f"({head_tokens} live head-tokens per round), float64 C loops; rows"
+              f"{' and key heads' if by_head else ''} run as {len(pieces)} independent "
+              f"pieces on {ncpu} threads: {all_r} rounds in {all_s:.1f} s; one thread: {one_r} rounds in "
+              f"{one_s:.1f} s")
+    return {"value": all_v, "unit": UNIT, "cores": ncpu, "kind": "oracle", "sample": sample,
+            "single_thread": {"value": one_v, "unit": UNIT, "cores": 1},
+            "host": {"nproc": ncpu, "cpu": model}}
+
+
+def _cpu_workloads():
+    """Secondary workloads that get a CPU baseline: (oracle pass, workload, tokens per row sampled)."""
+    from gated_deltanet_linear_gdr_gb300 import workloads as W
+    return {
+        # the prefill sample: each row's first 256 tokens (the whole rows take minutes)
+        "prefill": ("fwd", W.prefill, 256),
+        "verify_fold": ("verify_fold", W.verify_fold, None),
+        "gdp_snapshots": ("snapshots", W.gdp_snapshots, None),
+    }
+
+
+def cpu_baseline_decode(w, budget_s=5.0):
+    """The CPU oracle on whole decode batches, one thread and every host core."""
+    return cpu_baseline("fwd", w, budget_s)
 
 
 def run_gdr(args):
@@ -573,6 +748,11 @@ def run_gdr(args):
             line["secondary"] = {"error": repr(e)}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(w)
+        sec = line.get("secondary")
+        if isinstance(sec, dict) and "error" not in sec:
+            for name, (kind, wl, t_max) in _cpu_workloads().items():
+                if name in sec:
+                    sec[name]["cpu_baseline"] = cpu_baseline(kind, wl(), t_max=t_max)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -585,30 +765,31 @@ DECODE_WORKLOAD = ("decode: batch 256 rows x 1 token (248 live, 8 padding slot -
 
 
 def run_reference(args):
-    """The CPU oracle as it stands, on the decode workload (rank 0 only)."""
+    """The CPU oracle as it stands, on the decode workload, on every host core
+    (rank 0 only): each step runs the whole decode batch as independent rows
+    on one thread per core."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import oracle
     from gated_deltanet_linear_gdr_gb300 import workloads as W
     w = W.decode()
-    pool = w.state_pool(w.live_slots())
+    ncpu, model = host_cpu()
+    pieces = [cpu_piece(w, [b]) for b in range(w.batch)]
 
-    def one():
-        p = oracle.Problem(w.qkv, w.decay, w.beta, pool.copy(), w.slot_idx, w.offsets,
-                           nk=w.nk, nv=w.nv, K=w.K, V=w.V)
-        t0 = time.perf_counter()
-        oracle.fwd(p)
-        return time.perf_counter() - t0
+    def run_piece(pc):
+        args_ = dict(pc)
+        args_["state"] = args_["state"].copy()
+        oracle.fwd(oracle.Problem(**args_))
 
     for _ in range(max(1, args.warmup)):
-        one()
-    times = [one() for _ in range(args.steps)]
+        _cpu_time(pieces, run_piece, ncpu)
+    times = [_cpu_time(pieces, run_piece, ncpu) for _ in range(args.steps)]
     total = sum(times)
     ht = w.live_head_tokens
     value = ht * args.steps / total
-    sample = (f"whole decode batch per step (256 rows, {ht} live head-tokens), float64 C loops, "
-              f"single thread")
+    sample = (f"whole decode batch per step (256 rows, {ht} live head-tokens), float64 C loops, rows as "
+              f"independent pieces on {ncpu} threads")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
@@ -616,14 +797,74 @@ def run_reference(args):
         "data": "synthetic", "impl": "reference",
         "config": {"workload": DECODE_WORKLOAD, "global_batch": 256, "seq_len": 1, "parallelism": "dp1",
                    "runs_on": "host cores (the CPU oracle)"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": ncpu, "kind": "oracle", "sample": sample,
+                         "host": {"nproc": ncpu, "cpu": model}},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+def copy_bandwidth(steps=20):
+    """Pinned host<->device copy bandwidth against copy size: one cudaMemcpyAsync
+    per copy on its own stream, CUDA events around it, median of `steps`; also
+    both directions at once on two streams (the overlap gdr_fwd_host uses)."""
+    import torch
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    rows = []
+    decode_in = DECODE_H2D_BYTES
+    sizes = sorted({64 << 10, 256 << 10, 1 << 20, 4 << 20, decode_in, 16 << 20, 64 << 20, 256 << 20})
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    for n in sizes:
+        h_in = torch.empty(n // 4, dtype=torch.float32).pin_memory()
+        h_out = torch.empty(n // 4, dtype=torch.float32).pin_memory()
+        d_a = torch.empty(n // 4, dtype=torch.float32, device=dev)
+        d_b = torch.empty(n // 4, dtype=torch.float32, device=dev)
+
+        def timed(fn, stream):
+            ts = []
+            for _ in range(steps + 3):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b))
+            return statistics.median(ts[3:]) * 1e-3
+
+        with torch.cuda.stream(s1):
+            t_h2d = timed(lambda: d_a.copy_(h_in, non_blocking=True), s1)
+            t_d2h = timed(lambda: h_out.copy_(d_b, non_blocking=True), s1)
+
+        def both():
+            e = torch.cuda.Event()
+            e.record(s1)
+            s2.wait_event(e)
+            with torch.cuda.stream(s1):
+                d_a.copy_(h_in, non_blocking=True)
+            with torch.cuda.stream(s2):
+                h_out.copy_(d_b, non_blocking=True)
+            f = torch.cuda.Event()
+            f.record(s2)
+            s1.wait_event(f)
+        t_both = timed(both, s1)
+        rows.append({"bytes": n, "h2d_gbs": n / t_h2d / 1e9, "d2h_gbs": n / t_d2h / 1e9,
+                     "h2d_us": t_h2d * 1e6, "d2h_us": t_d2h * 1e6,
+                     "both_directions_gbs": 2 * n / t_both / 1e9})
+    print(json.dumps({"copy_bandwidth": rows, "pinned": True,
+                      "method": "one cudaMemcpyAsync per copy, CUDA events on its stream, median of "
+                                f"{steps}"}), flush=True)
+
+
+# Pinned host bytes one decode step copies in (q/k/v, decay, beta, slot_idx, offsets).
+DECODE_H2D_BYTES = 256 * (2 * 16 * 128 + 32 * 128) * 4 + 2 * 256 * 32 * 4 + 256 * 4 + 257 * 4
+
+
 def main():
     args = parse()
+    if args.copy_bandwidth:
+        copy_bandwidth()
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     HostForward,
     gdr_fold,
     gdr_fwd,
+    gdr_fwd_conv,
     gdr_fwd_dense,
     gdr_fwd_snapshots,
     gdr_get_status,
@@ -24,6 +25,7 @@ from ._binding import (  # noqa: F401
     load_library,
     prepare_fold,
     prepare_fwd,
+    prepare_fwd_conv,
     prepare_fwd_snapshots,
     prepare_rollback,
     prepare_verify_ring,

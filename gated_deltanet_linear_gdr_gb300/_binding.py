@@ -65,6 +65,17 @@ class gdr_step_args(ctypes.Structure):
     ]
 
 
+class gdr_conv_args(ctypes.Structure):
+    """Mirror of struct gdr_conv_args in include/gdr.h."""
+    _fields_ = [
+        ("width", ctypes.c_int32), ("activation", ctypes.c_int32),
+        ("weight", ctypes.c_void_p), ("weight_chan_stride", ctypes.c_int64),
+        ("weight_tap_stride", ctypes.c_int64), ("bias", ctypes.c_void_p),
+        ("conv_state", ctypes.c_void_p), ("state_slot_stride", ctypes.c_int64),
+        ("state_chan_stride", ctypes.c_int64), ("state_tap_stride", ctypes.c_int64),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -91,6 +102,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                 "gdr_fwd_host": ([A, ctypes.POINTER(gdr_host_io), i32, vp, vp, vp], ctypes.c_int),
                 "gdr_fwd_host_noalloc": ([A, ctypes.POINTER(gdr_host_io), i32, vp, vp, vp], ctypes.c_int),
                 "gdr_fwd_dense": ([A, vp, vp, vp], ctypes.c_int),
+                "gdr_fwd_conv": ([A, ctypes.POINTER(gdr_conv_args), vp], ctypes.c_int),
                 "gdr_verify_ring": ([A, vp, i32, i64, i32, i64, vp, vp], ctypes.c_int),
                 "gdr_fold": ([A, vp, i32, i64, i32, i64, vp, vp, vp], ctypes.c_int),
                 "gdr_fwd_snapshots": ([A, vp, i64, i64, i64, i32, i32, vp], ctypes.c_int),
@@ -288,6 +300,74 @@ class HostForward:
         _check(load_library().gdr_fwd_host(ctypes.byref(self.args), ctypes.byref(io), self.chunks, s,
                                            self.h2d.cuda_stream, self.d2h.cuda_stream))
         return out
+
+
+def make_conv_args(weight, bias, conv_state, state, activation="silu") -> gdr_conv_args:
+    """Pack the Pass-1 convolution's tensors into gdr_conv_args: weight
+    [conv_dim, width] float32, bias [conv_dim] float32 or None, conv_state
+    [slots, conv_dim, width-1] float32 indexed like the pool `state` (None
+    when width == 1); activation "silu" or None."""
+    _dev(weight, "conv_weight", torch.float32)
+    if weight.dim() != 2:
+        raise ValueError("conv_weight must be [conv_dim, width]")
+    C, width = weight.shape
+    c = gdr_conv_args()
+    c.width = width
+    if activation not in (None, "silu"):
+        raise ValueError('activation must be "silu" or None')
+    c.activation = 1 if activation == "silu" else 0
+    c.weight = weight.data_ptr()
+    c.weight_chan_stride, c.weight_tap_stride = weight.stride()
+    if bias is not None:
+        _dev(bias, "conv_bias", torch.float32)
+        if bias.shape != (C,) or bias.stride() != (1,):
+            raise ValueError("conv_bias must be a contiguous [conv_dim] tensor")
+        c.bias = bias.data_ptr()
+    if width > 1:
+        if conv_state is None:
+            raise ValueError("conv_state is needed for width > 1")
+        _dev(conv_state, "conv_state", torch.float32)
+        if conv_state.dim() != 3 or conv_state.shape[1:] != (C, width - 1):
+            raise ValueError(f"conv_state must be [slots, {C}, {width - 1}]")
+        if conv_state.shape[0] < state.shape[0]:
+            raise ValueError("conv_state needs one row per pool slot (it is indexed by slot_idx)")
+        c.conv_state = conv_state.data_ptr()
+        c.state_slot_stride, c.state_chan_stride, c.state_tap_stride = conv_state.stride()
+    return c
+
+
+def gdr_fwd_conv(x, decay, beta, state, slot_idx, offsets, conv_weight, conv_bias=None, conv_state=None,
+                 activation="silu", out=None, *, decay_is_log=False, use_qk_l2norm=True, scale=0.0, eps=1e-6,
+                 max_row_len=0):
+    """Forward pass on the raw Pass-1 input x [T, 2*nk*K + nv*V]: the causal
+    depthwise convolution ("gated_delta_recurrence_fwd_gpu", Args:
+    qkv_conv_output is the Conv1d output from Pass 1) fused into the
+    recurrence's operand staging; state and conv_state updated in place;
+    returns out."""
+    if out is None:
+        out = torch.empty(gdr_output_shape(x.shape[0], state.shape[1], state.shape[3]),
+                          dtype=torch.float32, device=x.device)
+    a = make_args(x, decay, beta, state, slot_idx, offsets, out, nk=_nk_from_qkv(x, state),
+                  decay_is_log=decay_is_log, use_qk_l2norm=use_qk_l2norm, scale=scale, eps=eps,
+                  max_row_len=max_row_len)
+    if conv_weight.shape[0] != x.shape[1]:
+        raise ValueError("conv_weight must have one row per input channel")
+    c = make_conv_args(conv_weight, conv_bias, conv_state, state, activation)
+    _check(load_library().gdr_fwd_conv(ctypes.byref(a), ctypes.byref(c), _stream(x.device)))
+    return out
+
+
+def prepare_fwd_conv(x, decay, beta, state, slot_idx, offsets, conv_weight, conv_bias, conv_state, out, *,
+                     activation="silu", decay_is_log=False, use_qk_l2norm=True, scale=0.0, eps=1e-6,
+                     max_row_len=0) -> "Prepared":
+    a = make_args(x, decay, beta, state, slot_idx, offsets, out, nk=_nk_from_qkv(x, state),
+                  decay_is_log=decay_is_log, use_qk_l2norm=use_qk_l2norm, scale=scale, eps=eps,
+                  max_row_len=max_row_len)
+    c = make_conv_args(conv_weight, conv_bias, conv_state, state, activation)
+    lib = load_library()
+    return Prepared(lambda ap, cp, s: lib.gdr_fwd_conv(ap, cp, s), a, (ctypes.byref(c),),
+                    (x, decay, beta, state, slot_idx, offsets, out, conv_weight, conv_bias, conv_state, c),
+                    x.device)
 
 
 def gdr_fwd_dense(qkv, decay, beta, offsets, initial_state=None, output_final_state=True, out=None, *,

@@ -475,6 +475,43 @@ int gdr_fwd_host_noalloc(const gdr_step_args *a, const gdr_host_io *h, int32_t c
     return gdr_fwd_host(&g, h, chunks, stream, h2d_stream, d2h_stream);
 }
 
+int gdr_fwd_conv(const gdr_step_args *a, const gdr_conv_args *c, void *stream) {
+    const char *fn = "gdr_fwd_conv";
+    int rc = check_step(a, fn);
+    if (rc) return rc;
+    if (!c) return fail(GDR_ERR_INVALID_ARG, "%s: conv is NULL", fn);
+    if (a->V != a->K) return fail(GDR_ERR_UNSUPPORTED, "%s: V=%d must equal K=%d", fn, a->V, a->K);
+    if (a->beta_vdim_stride > 0)
+        return fail(GDR_ERR_UNSUPPORTED, "%s: beta must be [total_tokens, nv] (beta_vdim_stride 0)", fn);
+    if (c->width < 1 || c->width > 4) return fail(GDR_ERR_UNSUPPORTED, "%s: width %d not in [1, 4]", fn, c->width);
+    if (c->activation != 0 && c->activation != 1)
+        return fail(GDR_ERR_INVALID_ARG, "%s: activation %d (0 none, 1 SiLU)", fn, c->activation);
+    if (!c->weight || c->weight_chan_stride <= 0 || c->weight_tap_stride <= 0)
+        return fail(GDR_ERR_INVALID_ARG, "%s: weight is NULL or has a non-positive stride", fn);
+    if (c->width > 1 && a->batch > 0 &&
+        (!c->conv_state || c->state_slot_stride <= 0 || c->state_chan_stride <= 0 || c->state_tap_stride <= 0))
+        return fail(GDR_ERR_INVALID_ARG, "%s: conv_state is NULL or has a non-positive stride", fn);
+    if (a->batch == 0) return ok();
+    unsigned *st = nullptr;
+    if ((rc = status_ptr(&st))) return rc;
+    const gdr::StepParams p = lower(a, st);
+    gdr::ConvParams cv{};
+    cv.width = c->width;
+    cv.silu = c->activation;
+    cv.w = c->weight;
+    cv.w_cs = c->weight_chan_stride;
+    cv.w_ts = c->weight_tap_stride;
+    cv.bias = c->bias;
+    cv.state = c->conv_state;
+    cv.cs_slot = c->state_slot_stride;
+    cv.cs_chan = c->state_chan_stride;
+    cv.cs_tap = c->state_tap_stride;
+    cv.channels = 2 * a->nk * a->K + a->nv * a->V;
+    return launched(gdr::launch_chain_conv(p, cv, a->K, a->state_dtype == GDR_BF16, a->max_row_len,
+                                           static_cast<cudaStream_t>(stream)),
+                    fn);
+}
+
 int gdr_fwd_dense(const gdr_step_args *a, const void *initial_state, void *final_state, void *stream) {
     const char *fn = "gdr_fwd_dense";
     if (!a) return fail(GDR_ERR_INVALID_ARG, "%s: args is NULL", fn);

@@ -94,6 +94,18 @@ struct RollbackParams {
     unsigned *status;
 };
 
+// Pass-1 convolution of the forward pass (gdr_fwd_conv): causal depthwise over
+// the conv_dim channels of the raw input staged from StepParams::qkv.
+struct ConvParams {
+    int width, silu;
+    const float *w;
+    long long w_cs, w_ts;
+    const float *bias;  // or null
+    float *state;       // [max_slots, conv_dim, width-1] float32 (null when width == 1)
+    long long cs_slot, cs_chan, cs_tap;
+    int channels;       // conv_dim
+};
+
 enum class Mode : int { Fwd = 0, Verify = 1, Snap = 2 };
 
 // Unsigned division by a divisor fixed at launch, as a multiply-high, an add
@@ -163,5 +175,9 @@ cudaError_t launch_short(const StepParams &p, int K, bool bf16, Mode mode, const
                          const SnapParams &sp, long long max_row_len, cudaStream_t s, bool *used);
 cudaError_t launch_fold(const FoldParams &p, int K, bool bf16, cudaStream_t s);
 cudaError_t launch_rollback(const RollbackParams &p, int K, int V, bool bf16, cudaStream_t s);
+// The forward pass with the Pass-1 convolution fused into operand staging,
+// then the conv-state update (two launches on s).
+cudaError_t launch_chain_conv(const StepParams &p, const ConvParams &cp, int K, bool bf16, long long max_row_len,
+                              cudaStream_t s);
 
 }  // namespace gdr

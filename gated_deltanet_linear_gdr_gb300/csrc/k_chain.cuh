@@ -25,7 +25,7 @@ namespace gdr {
 // Tokens per staged chunk TCX (8, 16 or 32, chosen by the launcher from the
 // caller's row-length bound); per-element beta (BPV) stages beta per token
 // like v and uses at most 8 tokens.
-template <typename ST, int K, int VV = K, bool BPV = false, int TCX = 16> struct ChainShape {
+template <typename ST, int K, int VV = K, bool BPV = false, int TCX = 16, bool CONV = false> struct ChainShape {
     static constexpr int V = VV;                   // value head size: K, 2K or K/2
     static constexpr int NG = K / 8;               // row groups
     // lanes along K: 4 (32 rows per lane at K = 128), or 2 for K = 128 with
@@ -54,7 +54,12 @@ template <typename ST, int K, int VV = K, bool BPV = false, int TCX = 16> struct
     // {alpha, beta, k^.q~, -} [2][TC][4]; per-element beta [2][TC][VS]
     static constexpr int SM_Q = 0, SM_K = SM_Q + 2 * TC * KP, SM_V = SM_K + 2 * TC * KP;
     static constexpr int SM_SC = SM_V + 2 * TC * VS, SM_B = SM_SC + 2 * TC * 4;
-    static constexpr int SMEM = (SM_B + (BPV ? 2 * TC * VS : 0)) * 4;  // bytes
+    // Pass-1 convolution (CONV): the CTA's channels -- its key head's q and k,
+    // its value slice -- each with width taps (zero-filled to 4), bias and the
+    // last 3 raw inputs, [NCH][8] floats, owned by one thread each
+    static constexpr int NCH = 2 * K + VS;
+    static constexpr int SM_CV = SM_B + (BPV ? 2 * TC * VS : 0);
+    static constexpr int SMEM = (SM_CV + (CONV ? NCH * 8 : 0)) * 4;  // bytes
     static constexpr int NL = NG / (RPAIR ? 2 : 1);  // lanes per token when normalising
     static constexpr int TPW = 32 / NL;            // tokens per warp when normalising
     using State = LaneState<RG, C>;
@@ -62,6 +67,44 @@ template <typename ST, int K, int VV = K, bool BPV = false, int TCX = 16> struct
 
 // Shared-memory index of raw row i (natural order, padded every ROWS rows).
 template <int ROWS> __device__ __forceinline__ int pidx(int i) { return vpos<false, ROWS>(i); }
+
+// Global channel of the CTA's convolution channel j: its key head's q (j < K),
+// k (j < 2K), then its slice of value head h.
+template <int K, int V, int VS>
+__device__ __forceinline__ int conv_channel(int j, const StepParams &p, int hk, int h, int slice) {
+    if (j < K) return hk * K + j;
+    if (j < 2 * K) return p.nk * K + hk * K + (j - K);
+    return 2 * p.nk * K + h * V + slice * VS + (j - 2 * K);
+}
+
+// One channel's causal convolution over tc staged tokens (x0[t * xs]), in
+// place: y = bias, y = fma(w[m], xe[m], y) for the WW taps m = 0 .. WW-1 over
+// the window xe = (last WW-1 inputs, this input), then SiLU y / (1 + exp(-y))
+// when asked.  e = {taps 0..3, bias, history 0..2}; the history (the last
+// three raw inputs, oldest first) is carried to the next chunk in e.
+template <int WW>
+__device__ __forceinline__ void conv_run(float *x0, int xs, int tc, float *e, int silu) {
+    float w[WW], hst[WW > 1 ? WW - 1 : 1];
+#pragma unroll
+    for (int m = 0; m < WW; ++m) w[m] = e[m];
+#pragma unroll
+    for (int m = 0; m < WW - 1; ++m) hst[m] = e[5 + m];
+    const float bias = e[4];
+    for (int t = 0; t < tc; ++t) {
+        const float x = x0[t * xs];
+        float y = bias;
+#pragma unroll
+        for (int m = 0; m < WW - 1; ++m) y = __fmaf_rn(w[m], hst[m], y);
+        y = __fmaf_rn(w[WW - 1], x, y);
+        if (silu) y = __fdiv_rn(y, __fadd_rn(1.0f, expf(-y)));
+        x0[t * xs] = y;
+#pragma unroll
+        for (int m = 0; m + 1 < WW - 1; ++m) hst[m] = hst[m + 1];
+        if constexpr (WW > 1) hst[WW - 2] = x;
+    }
+#pragma unroll
+    for (int m = 0; m < WW - 1; ++m) e[5 + m] = hst[m];
+}
 
 // Block -> unit for a few long rows of unequal length (every thread of the
 // CTA calls it; needs blockDim.x >= batch).  A CTA owns its row for the whole
@@ -99,11 +142,12 @@ __device__ __forceinline__ long long chain_balanced_unit(const StepParams &p, in
 // registers; with 32-row lanes they already let the compiler keep more staged
 // operands in flight, ragged prefill 2.10 -> 2.02 ms).  The 64-row lane takes
 // the same cap with shorter chunks.
-template <typename ST, int K, int VV, Mode MODE, bool BPV, int TCX>
-__global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX>::NT,
-                                  (TCX >= 32 || ChainShape<ST, K, VV, BPV, TCX>::ROWS >= 64) ? 2 : 4)
-    k_chain(const StepParams p, const RingParams rp, const SnapParams sp, const long long max_len, const int order_p) {
-    using Sh = ChainShape<ST, K, VV, BPV, TCX>;
+template <typename ST, int K, int VV, Mode MODE, bool BPV, int TCX, bool CONV = false>
+__global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX, CONV>::NT,
+                                  (TCX >= 32 || ChainShape<ST, K, VV, BPV, TCX, CONV>::ROWS >= 64) ? 2 : 4)
+    k_chain(const StepParams p, const RingParams rp, const SnapParams sp, const ConvParams cv, const long long max_len,
+            const int order_p) {
+    using Sh = ChainShape<ST, K, VV, BPV, TCX, CONV>;
     constexpr int V = VV, LK = Sh::LK, ROWS = Sh::ROWS, C = Sh::C;
     constexpr int WC = Sh::WC, W = Sh::W, NT = Sh::NT, VS = Sh::VS, SLICES = Sh::SLICES;
     constexpr int KP = Sh::KP, TC = Sh::TC, NL = Sh::NL, TPW = Sh::TPW;
@@ -161,6 +205,25 @@ __global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX>::NT,
                 records = true;
                 ring_row = ((long long)rs * p.nk + hk) * rp.len * rp.stride;
             }
+        }
+    }
+
+    // Pass-1 convolution: thread tid owns the CTA's channels j = tid, tid + NT,
+    // ... < NCH (q, then k, then the value slice); their taps, bias and the
+    // slot's conv state (the last width-1 raw inputs) go to shared memory
+    float *cv_s = chain_smem + Sh::SM_CV;  // [NCH][8]: taps 0..3, bias, history 0..2
+    if constexpr (CONV) {
+        for (int j = tid; j < Sh::NCH; j += NT) {
+            const int gc = conv_channel<K, V, Sh::VS>(j, p, hk, h, slice);
+            float *e = cv_s + j * 8;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) e[m] = m < cv.width ? cv.w[(long long)gc * cv.w_cs + m * cv.w_ts] : 0.0f;
+            e[4] = cv.bias ? cv.bias[gc] : 0.0f;
+#pragma unroll
+            for (int m = 0; m < 3; ++m)
+                e[5 + m] = m < cv.width - 1
+                               ? cv.state[(long long)slot * cv.cs_slot + (long long)gc * cv.cs_chan + m * cv.cs_tap]
+                               : 0.0f;
         }
     }
 
@@ -254,6 +317,22 @@ __global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX>::NT,
         float(*kb)[KP] = k_s[bi];
         float(*vb)[VS] = v_s[bi];
         float(*sb)[4] = sc_s[bi];
+        // ---- Pass-1 convolution of the staged raw inputs, in place, channel by
+        // channel in token order (each thread owns its channels' history)
+        if constexpr (CONV) {
+            for (int j = tid; j < Sh::NCH; j += NT) {
+                float *x0 = j < K ? &qb[0][pidx<ROWS>(j)] : j < 2 * K ? &kb[0][pidx<ROWS>(j - K)] : &vb[0][j - 2 * K];
+                const int xs = j < 2 * K ? KP : VS;
+                float *e = cv_s + j * 8;
+                switch (cv.width) {
+                    case 1: conv_run<1>(x0, xs, tc, e, cv.silu); break;
+                    case 2: conv_run<2>(x0, xs, tc, e, cv.silu); break;
+                    case 3: conv_run<3>(x0, xs, tc, e, cv.silu); break;
+                    default: conv_run<4>(x0, xs, tc, e, cv.silu); break;
+                }
+            }
+            __syncthreads();
+        }
         // ---- normalise: NL lanes per token; warp w takes tokens w, w + W, ...
         const bool rec_alpha = records && slice == 0, rec_k = rec_alpha && jr == 0;
         for (int tb = 0; tb < tc; tb += W * TPW) {
@@ -362,23 +441,23 @@ cudaError_t launch_chain_snap(const StepParams &p, int K, int V, bool bf16, cons
 
 // Launches one instantiation with its dynamic shared memory (opted in once per
 // device above 48 KiB); blocks = batch * nv * SLICES of that instantiation.
-template <typename ST, int K, int V, Mode MODE, bool BPV, int TCX>
+template <typename ST, int K, int V, Mode MODE, bool BPV, int TCX, bool CONV = false>
 inline cudaError_t launch_chain_k(const StepParams &p, const RingParams &rp, const SnapParams &sp,
-                                  long long max_len, cudaStream_t st) {
-    using Sh = ChainShape<ST, K, V, BPV, TCX>;
+                                  long long max_len, cudaStream_t st, const ConvParams &cv = ConvParams{}) {
+    using Sh = ChainShape<ST, K, V, BPV, TCX, CONV>;
     const long long blocks = (long long)p.batch * p.nv * Sh::SLICES;
     if (blocks <= 0) return cudaGetLastError();
     if (blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
     static LaunchCache cache;
     LaunchInfo li;
     cudaError_t e = launch_info(cache, &li, [](LaunchInfo &) {
-        return cudaFuncSetAttribute(k_chain<ST, K, V, MODE, BPV, TCX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Sh::SMEM);
+        return cudaFuncSetAttribute(k_chain<ST, K, V, MODE, BPV, TCX, CONV>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
     });
     if (e != cudaSuccess) return e;
     // a few rows: deal them out longest first (chain_balanced_unit)
     const int order_p = (p.batch <= Sh::NT && p.batch <= kChainOrderRows && blocks > li.sms) ? li.sms : 0;
-    k_chain<ST, K, V, MODE, BPV, TCX><<<(unsigned)blocks, Sh::NT, Sh::SMEM, st>>>(p, rp, sp, max_len, order_p);
+    k_chain<ST, K, V, MODE, BPV, TCX, CONV><<<(unsigned)blocks, Sh::NT, Sh::SMEM, st>>>(p, rp, sp, cv, max_len, order_p);
     return cudaGetLastError();
 }
 

@@ -230,6 +230,28 @@ def random_case(seed: int, lengths, nk: int, nv: int, K: int, max_slots: int,
                     use_l2norm=use_l2norm, scale=scale)
 
 
+@dataclass
+class ConvInputs:
+    """Pass-1 convolution parameters for a workload: weight [C, width], bias [C]
+    (or None), conv-state pool [slots, C, width-1] (None for width 1)."""
+    weight: np.ndarray
+    bias: Optional[np.ndarray]
+    state: Optional[np.ndarray]
+    silu: bool
+
+
+def conv_inputs(w: Workload, width: int = 4, seed: int = 0, bias: bool = True, silu: bool = True,
+                weight_std: float = 0.5) -> ConvInputs:
+    """Seeded Pass-1 convolution parameters for workload w: taps ~ N(0, weight_std^2),
+    bias ~ N(0, 0.1^2), conv state ~ N(0, 1) (the raw inputs' scale)."""
+    rng = np.random.default_rng([seed, 4049, width])
+    C = w.qkv.shape[1]
+    wt = (rng.standard_normal((C, width), dtype=np.float32) * np.float32(weight_std))
+    b = rng.standard_normal(C, dtype=np.float32) * np.float32(0.1) if bias else None
+    st = rng.standard_normal((w.max_slots, C, width - 1), dtype=np.float32) if width > 1 else None
+    return ConvInputs(wt, b, st, silu)
+
+
 CONFIGS = {
     "tiny": tiny,
     "decode": decode,

@@ -233,6 +233,46 @@ int gdr_fwd_host(const gdr_step_args *args, const gdr_host_io *host, int32_t chu
 int gdr_fwd_host_noalloc(const gdr_step_args *args, const gdr_host_io *host, int32_t chunks, void *stream,
                          void *h2d_stream, void *d2h_stream);
 
+/*
+ * Pass-1 convolution of gdr_fwd_conv ("gated_delta_recurrence_fwd_gpu", Args:
+ * qkv_conv_output is the "Conv1d output from Pass 1").  The pages give only
+ * the output's layout; the convolution is the causal depthwise one over the
+ * conv_dim = 2*nk*K + nv*V channels, every parameter from the caller: for
+ * token j of a row and channel c, with xe = the slot's conv state for c
+ * (oldest first) followed by the row's raw inputs x[t, c],
+ *     y[t0+j, c] = act(bias[c] + sum_m weight[c, m] * xe[j + m]),  m = 0 .. width-1
+ * (tap width-1 multiplies the newest input; act is the identity or SiLU
+ * y / (1 + exp(-y))), evaluated in float32 as y = bias, then
+ * y = fma(weight[c, m], xe[j + m], y) for m = 0, 1, ..., then the activation.
+ * The conv state pool [max_slots, conv_dim, width-1] is float32, indexed by
+ * the args' slot_idx like the recurrence pool, and replaced by the last
+ * width-1 entries of xe (a row shorter than width-1 keeps part of it);
+ * padding and empty rows leave it alone.
+ */
+typedef struct gdr_conv_args {
+    int32_t width;      /* taps per channel, 1 .. 4                                     */
+    int32_t activation; /* 0: none, 1: SiLU                                             */
+    const float *weight;          /* [conv_dim, width]: element (c, m) at               */
+    int64_t weight_chan_stride;   /*   c*weight_chan_stride + m*weight_tap_stride         */
+    int64_t weight_tap_stride;
+    const float *bias;            /* [conv_dim], unit stride, or NULL (no bias)          */
+    float *conv_state;            /* [max_slots, conv_dim, width-1]; NULL when width == 1 */
+    int64_t state_slot_stride;
+    int64_t state_chan_stride;
+    int64_t state_tap_stride;
+} gdr_conv_args;
+
+/* Forward pass on the RAW Pass-1 input ("gated_delta_recurrence_fwd_gpu" with
+ * its qkv_conv_output produced in the same call): args->qkv holds the
+ * convolution's input x [total_tokens, conv_dim] (same channel layout and
+ * strides as qkv_conv_output); the kernel convolves each staged chunk of
+ * tokens as it stages them (the convolution output is never written to
+ * memory), runs the recurrence exactly as gdr_fwd on the result, and then
+ * replaces every live row's conv state.  V = K and head-wise beta only.  A
+ * width-1 filter of weight 1, no bias and no activation gives gdr_fwd's
+ * results bit for bit.  The conv state must not alias any other buffer. */
+int gdr_fwd_conv(const gdr_step_args *args, const gdr_conv_args *conv, void *stream);
+
 /* Forward pass with a dense start and end state ("core.ssm.ops.gdp.fused_recurrent",
  * initial_state [N, HV, K, V] or None for zeros, output_final_state): as gdr_fwd,
  * but row b starts from initial_state[b] (zeros when initial_state is NULL) and

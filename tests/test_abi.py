@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ["gdr_fwd", "gdr_verify_ring", "gdr_fold", "gdr_fwd_snapshots", "gdr_rollback",
+    for n in ["gdr_fwd", "gdr_fwd_conv", "gdr_verify_ring", "gdr_fold", "gdr_fwd_snapshots", "gdr_rollback",
               "gdr_output_shape", "gdr_ring_record_elements", "gdr_last_error", "gdr_get_status"]:
         assert n in names
 
@@ -49,22 +49,23 @@ def test_library_exports_nothing_else(lib):
     assert syms == set(declared_functions()), syms ^ set(declared_functions())
 
 
-def test_struct_layout_matches_header(tmp_path):
+@pytest.mark.parametrize("cls,name", [(B.gdr_step_args, "gdr_step_args"), (B.gdr_conv_args, "gdr_conv_args")])
+def test_struct_layout_matches_header(tmp_path, cls, name):
     """The ctypes mirror has the C compiler's size and field offsets for the
     struct in include/gdr.h."""
-    fields = [f[0] for f in B.gdr_step_args._fields_]
+    fields = [f[0] for f in cls._fields_]
     prog = tmp_path / "layout.c"
     prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gdr.h"\nint main(void) {\n'
-                    '  printf("size %zu\\n", sizeof(gdr_step_args));\n' +
-                    "".join(f'  printf("{f} %zu\\n", offsetof(gdr_step_args, {f}));\n' for f in fields) +
+                    f'  printf("size %zu\\n", sizeof({name}));\n' +
+                    "".join(f'  printf("{f} %zu\\n", offsetof({name}, {f}));\n' for f in fields) +
                     "  return 0;\n}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
     got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
                                                         check=True).stdout.splitlines())
-    assert int(got["size"]) == ctypes.sizeof(B.gdr_step_args)
+    assert int(got["size"]) == ctypes.sizeof(cls)
     for f in fields:
-        assert int(got[f]) == getattr(B.gdr_step_args, f).offset, f
+        assert int(got[f]) == getattr(cls, f).offset, f
 
 
 def test_helpers(lib):
@@ -241,6 +242,37 @@ def test_binding_rejects_short_intermediate_buffer():
     with pytest.raises(ValueError, match="slot rows"):
         B._inter_strides(torch.zeros((5, 3, 2, 16, 16)), state)
     assert B._inter_strides(torch.zeros((6, 3, 2, 16, 16)), state)[3] == 3
+
+
+def test_fwd_conv_rejects_bad_arguments(lib):
+    a = _valid_args()
+    a.state_dtype = B.GDR_F32
+    fake = 0x7f0000000000
+    c = B.gdr_conv_args()
+    c.width, c.activation = 4, 1
+    c.weight, c.weight_chan_stride, c.weight_tap_stride = fake, 4, 1
+    c.conv_state = fake
+    c.state_slot_stride, c.state_chan_stride, c.state_tap_stride = 96 * 3, 3, 1
+    assert lib.gdr_fwd_conv(ctypes.byref(a), None, None) == B.GDR_ERR_INVALID_ARG
+    for field, value, code in [("width", 0, B.GDR_ERR_UNSUPPORTED), ("width", 5, B.GDR_ERR_UNSUPPORTED),
+                               ("activation", 2, B.GDR_ERR_INVALID_ARG), ("weight", None, B.GDR_ERR_INVALID_ARG),
+                               ("weight_tap_stride", 0, B.GDR_ERR_INVALID_ARG),
+                               ("conv_state", None, B.GDR_ERR_INVALID_ARG),
+                               ("state_chan_stride", 0, B.GDR_ERR_INVALID_ARG)]:
+        bad = B.gdr_conv_args.from_buffer_copy(c)
+        setattr(bad, field, value)
+        assert lib.gdr_fwd_conv(ctypes.byref(a), ctypes.byref(bad), None) == code, field
+    # width 1 needs no conv state
+    one = B.gdr_conv_args.from_buffer_copy(c)
+    one.width, one.conv_state = 1, None
+    a.batch = 0
+    assert lib.gdr_fwd_conv(ctypes.byref(a), ctypes.byref(one), None) == B.GDR_OK
+    a.batch = 2
+    a.V = 32  # the fused convolution takes V = K only
+    assert lib.gdr_fwd_conv(ctypes.byref(a), ctypes.byref(c), None) == B.GDR_ERR_UNSUPPORTED
+    a.V = 16
+    a.beta_seq_stride, a.beta_head_stride, a.beta_vdim_stride = 64, 16, 1
+    assert lib.gdr_fwd_conv(ctypes.byref(a), ctypes.byref(c), None) == B.GDR_ERR_UNSUPPORTED
 
 
 def test_empty_batch_is_a_no_op(lib):

@@ -54,12 +54,14 @@ template <typename ST, int K, int VV = K, bool BPV = false, int TCX = 16, bool C
     // {alpha, beta, k^.q~, -} [2][TC][4]; per-element beta [2][TC][VS]
     static constexpr int SM_Q = 0, SM_K = SM_Q + 2 * TC * KP, SM_V = SM_K + 2 * TC * KP;
     static constexpr int SM_SC = SM_V + 2 * TC * VS, SM_B = SM_SC + 2 * TC * 4;
-    // Pass-1 convolution (CONV): the CTA's channels -- its key head's q and k,
-    // its value slice -- each with width taps (zero-filled to 4), bias and the
-    // last 3 raw inputs, [NCH][8] floats, owned by one thread each
+    // Pass-1 convolution (CONV): the taps (zero-filled to 4) and bias of each
+    // of the CTA's channels -- its key head's q and k, its value slice --
+    // [NCH][5] floats; thread tid owns channels tid, tid + NT, ... (CPT of
+    // them) and keeps their last 3 raw inputs in registers
     static constexpr int NCH = 2 * K + VS;
+    static constexpr int CPT = (NCH + NT - 1) / NT;
     static constexpr int SM_CV = SM_B + (BPV ? 2 * TC * VS : 0);
-    static constexpr int SMEM = (SM_CV + (CONV ? NCH * 8 : 0)) * 4;  // bytes
+    static constexpr int SMEM = (SM_CV + (CONV ? NCH * 5 : 0)) * 4;  // bytes
     static constexpr int NL = NG / (RPAIR ? 2 : 1);  // lanes per token when normalising
     static constexpr int TPW = 32 / NL;            // tokens per warp when normalising
     using State = LaneState<RG, C>;
@@ -77,33 +79,87 @@ __device__ __forceinline__ int conv_channel(int j, const StepParams &p, int hk, 
     return 2 * p.nk * K + h * V + slice * VS + (j - 2 * K);
 }
 
-// One channel's causal convolution over tc staged tokens (x0[t * xs]), in
-// place: y = bias, y = fma(w[m], xe[m], y) for the WW taps m = 0 .. WW-1 over
-// the window xe = (last WW-1 inputs, this input), then SiLU y / (1 + exp(-y))
-// when asked.  e = {taps 0..3, bias, history 0..2}; the history (the last
-// three raw inputs, oldest first) is carried to the next chunk in e.
-template <int WW>
-__device__ __forceinline__ void conv_run(float *x0, int xs, int tc, float *e, int silu) {
-    float w[WW], hst[WW > 1 ? WW - 1 : 1];
+// The causal convolution of one staged chunk of tc tokens, in place, for the
+// thread's channels j = tid + i NT (Sh::CPT of them): per token and channel
+// y = bias, y = fma(w[m], xe[m], y) for the WW taps m = 0 .. WW-1 over the
+// window xe = (last WW-1 raw inputs, this input), then SiLU y / (1 + e^-y)
+// (fast exponential and division) when asked.  Taps and bias from cv_s
+// [NCH][5]; hist[i] holds channel i's last raw inputs, the newest last, and
+// is carried to the next chunk.  Channel j's staged values: q for j < K, k
+// for j < 2K, then the value slice.
+template <typename Sh, int WW>
+__device__ __forceinline__ void conv_chunk(float (*qb)[Sh::KP], float (*kb)[Sh::KP], float (*vb)[Sh::VS],
+                                           const float *cv_s, float (&hist)[Sh::CPT][3], int tc, int silu) {
+    constexpr int K = Sh::NG * 8, NCH = Sh::NCH, CPT = Sh::CPT, NT = Sh::NT;
+    const int tid = threadIdx.x;
+    float *x0[CPT];
+    int xs[CPT];
+    float w[CPT][4], bias[CPT];
 #pragma unroll
-    for (int m = 0; m < WW; ++m) w[m] = e[m];
+    for (int i = 0; i < CPT; ++i) {
+        const int j = min(tid + i * NT, NCH - 1);
+        x0[i] = j < K ? &qb[0][pidx<Sh::ROWS>(j)] : j < 2 * K ? &kb[0][pidx<Sh::ROWS>(j - K)] : &vb[0][j - 2 * K];
+        xs[i] = j < 2 * K ? Sh::KP : Sh::VS;
 #pragma unroll
-    for (int m = 0; m < WW - 1; ++m) hst[m] = e[5 + m];
-    const float bias = e[4];
-    for (int t = 0; t < tc; ++t) {
-        const float x = x0[t * xs];
-        float y = bias;
-#pragma unroll
-        for (int m = 0; m < WW - 1; ++m) y = __fmaf_rn(w[m], hst[m], y);
-        y = __fmaf_rn(w[WW - 1], x, y);
-        if (silu) y = __fdiv_rn(y, __fadd_rn(1.0f, expf(-y)));
-        x0[t * xs] = y;
-#pragma unroll
-        for (int m = 0; m + 1 < WW - 1; ++m) hst[m] = hst[m + 1];
-        if constexpr (WW > 1) hst[WW - 2] = x;
+        for (int m = 0; m < 4; ++m) w[i][m] = cv_s[j * 5 + m];
+        bias[i] = cv_s[j * 5 + 4];
     }
+    // blocks of TB tokens: every load of a block, then its TB * CPT
+    // independent outputs, then the stores (loads and stores go through
+    // pointers the compiler cannot tell apart, so it would keep them in order)
+    constexpr int TB = 4;
+    for (int t0 = 0; t0 < tc; t0 += TB) {
+        float xv[CPT][TB];
 #pragma unroll
-    for (int m = 0; m < WW - 1; ++m) e[5 + m] = hst[m];
+        for (int i = 0; i < CPT; ++i) {
+            const bool own = tid + i * NT < NCH;
+#pragma unroll
+            for (int u = 0; u < TB; ++u) xv[i][u] = own && t0 + u < tc ? x0[i][(t0 + u) * xs[i]] : 0.0f;
+        }
+        float yv[CPT][TB];
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+#pragma unroll
+            for (int u = 0; u < TB; ++u) {
+                // window: the last WW-1 inputs before token t0+u, then its own
+                float y = bias[i];
+#pragma unroll
+                for (int m = 0; m < WW - 1; ++m) {
+                    const int back = WW - 1 - m;  // inputs before this token
+                    const float xm = u - back >= 0 ? xv[i][u - back >= 0 ? u - back : 0] : hist[i][3 + u - back];
+                    y = __fmaf_rn(w[i][m], xm, y);
+                }
+                y = __fmaf_rn(w[i][WW - 1], xv[i][u], y);
+                if (silu) y = __fdividef(y, __fadd_rn(1.0f, __expf(-y)));
+                yv[i][u] = y;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            if (tid + i * NT < NCH) {
+#pragma unroll
+                for (int u = 0; u < TB; ++u)
+                    if (t0 + u < tc) x0[i][(t0 + u) * xs[i]] = yv[i][u];
+            }
+            // history: the last three inputs up to the block's last valid token
+            const int n = min(TB, tc - t0);
+            float nh[3];
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                // input at position n-3+m of the block (negative: from the old history)
+                float v = hist[i][m];
+#pragma unroll
+                for (int nn = 1; nn <= TB; ++nn)
+                    if (n == nn) {
+                        const int pos = nn - 3 + m;
+                        v = pos >= 0 ? xv[i][pos >= 0 ? pos : 0] : hist[i][3 + pos >= 0 ? 3 + pos : 0];
+                    }
+                nh[m] = v;
+            }
+#pragma unroll
+            for (int m = 0; m < 3; ++m) hist[i][m] = nh[m];
+        }
+    }
 }
 
 // Block -> unit for a few long rows of unequal length (every thread of the
@@ -208,22 +264,31 @@ __global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX, CONV>::NT,
         }
     }
 
-    // Pass-1 convolution: thread tid owns the CTA's channels j = tid, tid + NT,
-    // ... < NCH (q, then k, then the value slice); their taps, bias and the
-    // slot's conv state (the last width-1 raw inputs) go to shared memory
-    float *cv_s = chain_smem + Sh::SM_CV;  // [NCH][8]: taps 0..3, bias, history 0..2
+    // Pass-1 convolution: thread tid owns the CTA's channels j = tid + i NT
+    // < NCH (q, then k, then the value slice): their taps and bias go to
+    // shared memory, the slot's conv state (the last width-1 raw inputs, the
+    // newest last) to the thread's history registers
+    float *cv_s = chain_smem + Sh::SM_CV;  // [NCH][5]: taps 0..3, bias
+    float hist[Sh::CPT][3];
     if constexpr (CONV) {
-        for (int j = tid; j < Sh::NCH; j += NT) {
-            const int gc = conv_channel<K, V, Sh::VS>(j, p, hk, h, slice);
-            float *e = cv_s + j * 8;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) e[m] = m < cv.width ? cv.w[(long long)gc * cv.w_cs + m * cv.w_ts] : 0.0f;
-            e[4] = cv.bias ? cv.bias[gc] : 0.0f;
+        for (int i = 0; i < Sh::CPT; ++i) {
+            const int j = tid + i * NT;
+            if (j < Sh::NCH) {
+                const int gc = conv_channel<K, V, Sh::VS>(j, p, hk, h, slice);
 #pragma unroll
-            for (int m = 0; m < 3; ++m)
-                e[5 + m] = m < cv.width - 1
-                               ? cv.state[(long long)slot * cv.cs_slot + (long long)gc * cv.cs_chan + m * cv.cs_tap]
-                               : 0.0f;
+                for (int m = 0; m < 4; ++m)
+                    cv_s[j * 5 + m] = m < cv.width ? cv.w[(long long)gc * cv.w_cs + m * cv.w_ts] : 0.0f;
+                cv_s[j * 5 + 4] = cv.bias ? cv.bias[gc] : 0.0f;
+                // the width-1 stored inputs (oldest first) end at hist[i][2]
+#pragma unroll
+                for (int m = 0; m < 3; ++m) {
+                    const int si = m - (4 - cv.width);
+                    hist[i][m] = si >= 0 ? cv.state[(long long)slot * cv.cs_slot + (long long)gc * cv.cs_chan +
+                                                    si * cv.cs_tap]
+                                         : 0.0f;
+                }
+            }
         }
     }
 
@@ -317,19 +382,14 @@ __global__ void __launch_bounds__(ChainShape<ST, K, VV, BPV, TCX, CONV>::NT,
         float(*kb)[KP] = k_s[bi];
         float(*vb)[VS] = v_s[bi];
         float(*sb)[4] = sc_s[bi];
-        // ---- Pass-1 convolution of the staged raw inputs, in place, channel by
-        // channel in token order (each thread owns its channels' history)
+        // ---- Pass-1 convolution of the staged raw inputs, in place, token by
+        // token over the thread's channels (each thread owns its channels)
         if constexpr (CONV) {
-            for (int j = tid; j < Sh::NCH; j += NT) {
-                float *x0 = j < K ? &qb[0][pidx<ROWS>(j)] : j < 2 * K ? &kb[0][pidx<ROWS>(j - K)] : &vb[0][j - 2 * K];
-                const int xs = j < 2 * K ? KP : VS;
-                float *e = cv_s + j * 8;
-                switch (cv.width) {
-                    case 1: conv_run<1>(x0, xs, tc, e, cv.silu); break;
-                    case 2: conv_run<2>(x0, xs, tc, e, cv.silu); break;
-                    case 3: conv_run<3>(x0, xs, tc, e, cv.silu); break;
-                    default: conv_run<4>(x0, xs, tc, e, cv.silu); break;
-                }
+            switch (cv.width) {
+                case 1: conv_chunk<Sh, 1>(qb, kb, vb, cv_s, hist, tc, cv.silu); break;
+                case 2: conv_chunk<Sh, 2>(qb, kb, vb, cv_s, hist, tc, cv.silu); break;
+                case 3: conv_chunk<Sh, 3>(qb, kb, vb, cv_s, hist, tc, cv.silu); break;
+                default: conv_chunk<Sh, 4>(qb, kb, vb, cv_s, hist, tc, cv.silu); break;
             }
             __syncthreads();
         }

@@ -40,9 +40,10 @@ template <typename ST, int K>
 static cudaError_t conv_t(const StepParams &p, const ConvParams &cv, long long max_len, cudaStream_t st) {
     const RingParams rp{};
     const SnapParams sp{};
+    // the forward pass's chunk sizes: 8 tokens for rows bounded at 8, else kChainLongTC
     if (max_len >= 1 && max_len <= 8)
         return launch_chain_k<ST, K, K, Mode::Fwd, false, 8, true>(p, rp, sp, max_len, st, cv);
-    return launch_chain_k<ST, K, K, Mode::Fwd, false, 16, true>(p, rp, sp, max_len, st, cv);
+    return launch_chain_k<ST, K, K, Mode::Fwd, false, kChainLongTC, true>(p, rp, sp, max_len, st, cv);
 }
 
 cudaError_t launch_chain_conv(const StepParams &p, const ConvParams &cv, int K, bool bf16, long long max_row_len,

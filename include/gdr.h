@@ -243,7 +243,8 @@ int gdr_fwd_host_noalloc(const gdr_step_args *args, const gdr_host_io *host, int
  *     y[t0+j, c] = act(bias[c] + sum_m weight[c, m] * xe[j + m]),  m = 0 .. width-1
  * (tap width-1 multiplies the newest input; act is the identity or SiLU
  * y / (1 + exp(-y))), evaluated in float32 as y = bias, then
- * y = fma(weight[c, m], xe[j + m], y) for m = 0, 1, ..., then the activation.
+ * y = fma(weight[c, m], xe[j + m], y) for m = 0, 1, ..., then the activation
+ * (with the fast single-precision exponential and division: a few ulp).
  * The conv state pool [max_slots, conv_dim, width-1] is float32, indexed by
  * the args' slot_idx like the recurrence pool, and replaced by the last
  * width-1 entries of xe (a row shorter than width-1 keeps part of it);

@@ -79,6 +79,10 @@ __device__ __forceinline__ int conv_channel(int j, const StepParams &p, int hk, 
     return 2 * p.nk * K + h * V + slice * VS + (j - 2 * K);
 }
 
+template <bool B> struct WinFull {
+    static constexpr bool value = B;
+};
+
 // The causal convolution of one staged chunk of tc tokens, in place, for the
 // thread's channels j = tid + i NT (Sh::CPT of them): per token and channel
 // y = bias, y = fma(w[m], xe[m], y) for the WW taps m = 0 .. WW-1 over the
@@ -106,26 +110,31 @@ __device__ __forceinline__ void conv_chunk(float (*qb)[Sh::KP], float (*kb)[Sh::
     }
     // blocks of TB tokens: every load of a block, then its TB * CPT
     // independent outputs, then the stores (loads and stores go through
-    // pointers the compiler cannot tell apart, so it would keep them in order)
+    // pointers the compiler cannot tell apart, so it would keep them in
+    // order); whole blocks take a path without tail predicates
     constexpr int TB = 4;
-    for (int t0 = 0; t0 < tc; t0 += TB) {
-        float xv[CPT][TB];
+    bool own[CPT];
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) own[i] = tid + i * NT < NCH;
+    auto block = [&](auto full, int t0) {
+        constexpr bool FULL = decltype(full)::value;
+        const int n = FULL ? TB : tc - t0;
+        float xv[CPT][TB], yv[CPT][TB];
 #pragma unroll
         for (int i = 0; i < CPT; ++i) {
-            const bool own = tid + i * NT < NCH;
+            const float *px = x0[i] + t0 * xs[i];
 #pragma unroll
-            for (int u = 0; u < TB; ++u) xv[i][u] = own && t0 + u < tc ? x0[i][(t0 + u) * xs[i]] : 0.0f;
+            for (int u = 0; u < TB; ++u) xv[i][u] = own[i] && (FULL || u < n) ? px[u * xs[i]] : 0.0f;
         }
-        float yv[CPT][TB];
 #pragma unroll
         for (int i = 0; i < CPT; ++i) {
 #pragma unroll
             for (int u = 0; u < TB; ++u) {
-                // window: the last WW-1 inputs before token t0+u, then its own
+                // window: the WW-1 inputs before token t0+u, then its own
                 float y = bias[i];
 #pragma unroll
                 for (int m = 0; m < WW - 1; ++m) {
-                    const int back = WW - 1 - m;  // inputs before this token
+                    const int back = WW - 1 - m;
                     const float xm = u - back >= 0 ? xv[i][u - back >= 0 ? u - back : 0] : hist[i][3 + u - back];
                     y = __fmaf_rn(w[i][m], xm, y);
                 }
@@ -136,30 +145,39 @@ __device__ __forceinline__ void conv_chunk(float (*qb)[Sh::KP], float (*kb)[Sh::
         }
 #pragma unroll
         for (int i = 0; i < CPT; ++i) {
-            if (tid + i * NT < NCH) {
+            float *px = x0[i] + t0 * xs[i];
+            if (own[i]) {
 #pragma unroll
                 for (int u = 0; u < TB; ++u)
-                    if (t0 + u < tc) x0[i][(t0 + u) * xs[i]] = yv[i][u];
+                    if (FULL || u < n) px[u * xs[i]] = yv[i][u];
             }
-            // history: the last three inputs up to the block's last valid token
-            const int n = min(TB, tc - t0);
-            float nh[3];
+            // history: the last three inputs up to the block's last token
+            if constexpr (FULL) {
+                hist[i][0] = xv[i][TB - 3];
+                hist[i][1] = xv[i][TB - 2];
+                hist[i][2] = xv[i][TB - 1];
+            } else {
+                float nh[3];
 #pragma unroll
-            for (int m = 0; m < 3; ++m) {
-                // input at position n-3+m of the block (negative: from the old history)
-                float v = hist[i][m];
+                for (int m = 0; m < 3; ++m) {
+                    float v = hist[i][m];
 #pragma unroll
-                for (int nn = 1; nn <= TB; ++nn)
-                    if (n == nn) {
-                        const int pos = nn - 3 + m;
-                        v = pos >= 0 ? xv[i][pos >= 0 ? pos : 0] : hist[i][3 + pos >= 0 ? 3 + pos : 0];
-                    }
-                nh[m] = v;
+                    for (int nn = 1; nn < TB; ++nn)
+                        if (n == nn) {
+                            const int pos = nn - 3 + m;  // negative: from the old history
+                            v = pos >= 0 ? xv[i][pos >= 0 ? pos : 0] : hist[i][3 + pos >= 0 ? 3 + pos : 0];
+                        }
+                    nh[m] = v;
+                }
+#pragma unroll
+                for (int m = 0; m < 3; ++m) hist[i][m] = nh[m];
             }
-#pragma unroll
-            for (int m = 0; m < 3; ++m) hist[i][m] = nh[m];
         }
-    }
+    };
+    int t0 = 0;
+#pragma unroll 2
+    for (; t0 + TB <= tc; t0 += TB) block(WinFull<true>{}, t0);
+    if (t0 < tc) block(WinFull<false>{}, t0);
 }
 
 // Block -> unit for a few long rows of unequal length (every thread of the

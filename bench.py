@@ -56,6 +56,9 @@ def parse():
                     help="time just this secondary workload and print its figures (profiling aid)")
     ap.add_argument("--soak-s", type=float, default=1.0,
                     help="seconds of untimed steps after warm-up (steady clocks)")
+    ap.add_argument("--fma-probe", action="store_true",
+                    help="print the FP32-pipe rate of packed float32x2 arithmetic by register-operand pattern "
+                         "(the recurrence sweep's own sequence included) and exit")
     ap.add_argument("--copy-bandwidth", action="store_true",
                     help="print the pinned host<->device copy bandwidth against copy size and exit "
                          "(the link the end-to-end figure runs over)")
@@ -856,6 +859,57 @@ def copy_bandwidth(steps=20):
                                 f"{steps}"}), flush=True)
 
 
+def fma_probe(steps=7):
+    """FP32-pipe rate of packed float32x2 arithmetic with every operand in
+    registers, by operand pattern and warps per SM sub-partition (gdr_probe_fma):
+    the ceiling the recurrence kernels' fixed operation order can reach on the
+    FMA pipe.  CUDA events on the launching stream, median of `steps`, the SM
+    clock sampled during the runs."""
+    import torch
+    from gated_deltanet_linear_gdr_gb300 import GdrError, gdr_probe_fma
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    sink = torch.empty(sms * 128 * 8, dtype=torch.float32, device=dev)
+    # FP32 operations per thread per iteration, and iterations per launch
+    ops = {0: 512, 1: 16, 2: 16}
+    iters = {0: 1024, 1: 16384, 2: 16384}
+    names = {0: "recurrence sweep (t = alpha x; x = k u + t; a += x k; b += x q), 64 rows x 2 columns",
+             1: "packed FMA chains, multiplier and addend shared by every instruction",
+             2: "packed FMA chains, three distinct operand registers per instruction"}
+    clocks = ClockSampler(str(getattr(props, "uuid", "")))
+    clocks.start()
+    rows = []
+    for pattern in (1, 2, 0):
+        for w in (1, 2, 4, 8):
+            try:
+                gdr_probe_fma(pattern, w, iters[pattern], sink)
+            except GdrError:
+                continue  # the pattern's CTA does not fit one SM at this warp count
+            ts = []
+            for _ in range(steps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                ctas = gdr_probe_fma(pattern, w, iters[pattern], sink)
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b) * 1e-3)
+            t = statistics.median(ts)
+            n = ctas * 128 * w * iters[pattern] * ops[pattern]
+            rows.append({"pattern": pattern, "what": names[pattern], "warps_per_subpartition": w,
+                         "us": t * 1e6, "fp32_ops_per_s": n / t})
+    clk = clocks.stop()
+    mhz = clk.get("sm_mhz") or 2070.0
+    for r in rows:
+        r["ops_per_sm_per_cycle"] = r["fp32_ops_per_s"] / sms / (mhz * 1e6)
+        r["frac_of_fp32_peak"] = r["ops_per_sm_per_cycle"] / 128
+    print(json.dumps({"fma_probe": rows, "clocks": clk, "sms": sms,
+                      "peak": "128 FP32 lane operations per SM per cycle (an FMA or a multiply counts "
+                              "as one, as in the roofline's FMA-pipe count)"}), flush=True)
+
+
 # Pinned host bytes one decode step copies in (q/k/v, decay, beta, slot_idx, offsets).
 DECODE_H2D_BYTES = 256 * (2 * 16 * 128 + 32 * 128) * 4 + 2 * 256 * 32 * 4 + 256 * 4 + 257 * 4
 
@@ -864,6 +918,9 @@ def main():
     args = parse()
     if args.copy_bandwidth:
         copy_bandwidth()
+        return
+    if args.fma_probe:
+        fma_probe()
         return
     if args.impl == "reference":
         run_reference(args)

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     gdr_fwd_snapshots,
     gdr_get_status,
     gdr_output_shape,
+    gdr_probe_fma,
     gdr_ring_record_elements,
     gdr_rollback,
     gdr_verify_ring,

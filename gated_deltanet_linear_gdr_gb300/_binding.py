@@ -108,6 +108,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                 "gdr_fwd_snapshots": ([A, vp, i64, i64, i64, i32, i32, vp], ctypes.c_int),
                 "gdr_rollback": ([A, vp, i64, i64, i64, i32, vp, vp], ctypes.c_int),
                 "gdr_get_status": ([ctypes.POINTER(ctypes.c_uint32), i32], ctypes.c_int),
+                "gdr_probe_fma": ([i32, i32, i32, vp, i64, ctypes.POINTER(ctypes.c_int32), vp], ctypes.c_int),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -483,6 +484,20 @@ def gdr_get_status(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _check(load_library().gdr_get_status(ctypes.byref(v), int(bool(clear))))
     return int(v.value)
+
+
+def gdr_probe_fma(pattern: int, warps_per_subpartition: int, iterations: int, sink: torch.Tensor) -> int:
+    """Diagnostic FP32-pipe probe of include/gdr.h (pattern 0: the recurrence's
+    per-element sweep; 1: packed FMAs with reusable operands; 2: with three
+    distinct operands).  Launches on the current stream; returns the CTA count
+    (one per SM, 128 * warps_per_subpartition threads each)."""
+    _dev(sink, "sink", torch.float32)
+    if not sink.is_contiguous():
+        raise ValueError("sink must be contiguous")
+    ctas = ctypes.c_int32(0)
+    _check(load_library().gdr_probe_fma(int(pattern), int(warps_per_subpartition), int(iterations), sink.data_ptr(),
+                                        sink.numel(), ctypes.byref(ctas), _stream(sink.device)))
+    return int(ctas.value)
 
 
 def status_names(bits: int):

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdr.so")
 SOURCES = ["api.cu", "k_decode.cu", "k_short.cu", "k_chain.cu", "k_chain_fwd.cu", "k_chain_fwd_kv.cu", "k_chain_conv.cu", "k_chain_verify.cu",
-           "k_chain_snap.cu", "k_fold.cu"]
+           "k_chain_snap.cu", "k_fold.cu", "k_probe.cu"]
 HEADERS = ["gdr_internal.h", "gdr_device.cuh", "gdr_pipe.cuh", "gdr_state.cuh", "k_chain.cuh", "gdr.map"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

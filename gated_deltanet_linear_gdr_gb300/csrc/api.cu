@@ -662,6 +662,25 @@ int gdr_rollback(const gdr_step_args *a, const void *inter, int64_t inter_slot_s
                     "gdr_rollback");
 }
 
+int gdr_probe_fma(int32_t pattern, int32_t warps_per_subpartition, int32_t iterations, float *sink,
+                  int64_t sink_elements, int32_t *ctas, void *stream) {
+    if (pattern < 0 || pattern > 2 || warps_per_subpartition < 1 || warps_per_subpartition > 8 || iterations < 1 ||
+        !sink || !ctas)
+        return fail(GDR_ERR_INVALID_ARG, "gdr_probe_fma: invalid arguments");
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "gdr_probe_fma: %s", cudaGetErrorString(e));
+    if (sink_elements < (int64_t)sms * 128 * warps_per_subpartition)
+        return fail(GDR_ERR_INVALID_ARG, "gdr_probe_fma: sink holds %lld floats, %lld needed", (long long)sink_elements,
+                    (long long)sms * 128 * warps_per_subpartition);
+    e = gdr::launch_probe_fma(pattern, warps_per_subpartition, iterations, sink, static_cast<cudaStream_t>(stream), ctas);
+    if (e == cudaErrorInvalidConfiguration)
+        return fail(GDR_ERR_UNSUPPORTED, "gdr_probe_fma: pattern %d does not fit %d warps per sub-partition in one SM",
+                    pattern, warps_per_subpartition);
+    return launched(e, "gdr_probe_fma");
+}
+
 int gdr_get_status(uint32_t *status, int32_t clear) {
     if (!status) return fail(GDR_ERR_INVALID_ARG, "gdr_get_status: status is NULL");
     cudaError_t e = cudaDeviceSynchronize();

@@ -180,4 +180,8 @@ cudaError_t launch_rollback(const RollbackParams &p, int K, int V, bool bf16, cu
 cudaError_t launch_chain_conv(const StepParams &p, const ConvParams &cp, int K, bool bf16, long long max_row_len,
                               cudaStream_t s);
 
+// Diagnostic packed-FMA probes (k_probe.cu): one CTA of 128 * warps threads per
+// SM; *blocks_out receives the CTA count.
+cudaError_t launch_probe_fma(int pattern, int warps, int iters, float *sink, cudaStream_t st, int *blocks_out);
+
 }  // namespace gdr

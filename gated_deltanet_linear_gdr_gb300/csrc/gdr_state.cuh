@@ -110,6 +110,32 @@ template <int RG, int C> struct LaneState<RG, C, true> {
         fold_tree(pa, pb, a, b);
     }
 
+    // The two halves of advance: S <- alpha S, then S <- k^ u^T + S (the same
+    // roundings; the decay can then run while the reductions are reduced).
+    __device__ __forceinline__ void scale(float alpha) {
+        const float2 aa = make_float2(alpha, alpha);
+#pragma unroll
+        for (int gp = 0; gp < NP; ++gp)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int c = 0; c < C; ++c) x[gp][i][c] = __fmul2_rn(aa, x[gp][i][c]);
+    }
+    __device__ __forceinline__ void add_outer(const float *kv, const float (&u)[C]) {
+        float2 uu[C];
+#pragma unroll
+        for (int c = 0; c < C; ++c) uu[c] = make_float2(u[c], u[c]);
+#pragma unroll
+        for (int gp = 0; gp < NP; ++gp) {
+            float2 kp[8];
+            pairs(kv, gp, kp);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int c = 0; c < C; ++c) x[gp][i][c] = __ffma2_rn(kp[i], uu[c], x[gp][i][c]);
+        }
+    }
+
     // S <- k^ u^T + alpha S.
     __device__ __forceinline__ void advance(const float *kv, const float (&u)[C], float alpha) {
         const float2 aa = make_float2(alpha, alpha);
@@ -214,6 +240,15 @@ template <int RG, int C> struct LaneState<RG, C, false> {
         }
         fold_tree(pa, pb, a, b);
     }
+
+    __device__ __forceinline__ void scale(float alpha) {
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+            for (int c = 0; c < C; ++c) y[r][c] = __fmul_rn(alpha, y[r][c]);
+    }
+    // advance_cols with alpha = 1 adds k^ u^T with the same rounding (1 * S == S)
+    __device__ __forceinline__ void add_outer(const float *kv, const float (&u)[C]) { advance(kv, u, 1.0f); }
 
     __device__ __forceinline__ void advance(const float *kv, const float (&u)[C], float alpha) {
 #pragma unroll

@@ -291,6 +291,10 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
             const float alpha = ab[0], beta = ab[1], kq = ab[2];
             float a[C], bq[C];
             s.partials(tk + base, tq + base, a, bq);
+            // S <- alpha S now, independent of the reductions' tree; a verify
+            // row that does not commit never reads the state after its last token
+            const bool adv = commit || cb + tt + 1 < L;
+            if (adv) s.scale(alpha);
             const float *tv = tq + 2 * W::KP;
             float u[C], o[C];
 #pragma unroll
@@ -309,9 +313,8 @@ __device__ __forceinline__ bool short_compute(const StepParams &p, const RingPar
             }
             optr += p.out_ss;
             uidx += rp.stride;
-            // S <- k^ u^T + alpha S; a verify row that does not commit never
-            // reads the state after its last token
-            if (commit || cb + tt + 1 < L) s.advance(tk + base, u, alpha);
+            // S <- k^ u^T + S
+            if (adv) s.add_outer(tk + base, u);
         }
     }
     if (commit) short_put_tile<ST, K>(stage, r0, col, s);

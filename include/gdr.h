@@ -346,6 +346,31 @@ int gdr_rollback(const gdr_step_args *args, const void *inter, int64_t inter_slo
  * if clear != 0, resets it.  Synchronises the device. */
 int gdr_get_status(uint32_t *status, int32_t clear);
 
+/* Diagnostic, not part of the recurrence: measures how fast the FP32 pipe runs
+ * packed float32x2 arithmetic of a given register-operand pattern, every
+ * operand already in registers (no memory traffic).  It bounds what the
+ * recurrence kernels can reach on the FP32 pipe with their fixed operation
+ * order (the per-element decay multiply, rank-1 update and two reductions of
+ * "gated_delta_recurrence_fwd_gpu"'s per-token step).  Launches one CTA of
+ * 128 * warps_per_subpartition threads on every SM (*ctas receives the CTA
+ * count) on `stream`; each thread runs `iterations` iterations of:
+ *   pattern 0: the recurrence sweep on 64 rows x 2 columns -- per state
+ *              element pair t = alpha x; x = k^ u + t; a += x k'; b += x q'
+ *              (8-row chains) -- then a short dependent tail feeding the next
+ *              iteration: 256 packed instructions, 512 FP32 operations;
+ *   pattern 1: 8 independent packed FMA chains whose multiplier and addend
+ *              registers are the same in every instruction: 8 packed, 16 ops;
+ *   pattern 2: 8 independent packed FMA chains with three distinct operand
+ *              registers per instruction: 8 packed, 16 ops.
+ * Every thread writes one float to sink[cta * blockDim + thread]; sink must hold
+ * sink_elements >= SMs * 128 * warps_per_subpartition floats.  Time it with
+ * events on `stream`.  Returns GDR_ERR_UNSUPPORTED when the pattern's CTA does
+ * not fit one SM's registers at that warp count, GDR_ERR_INVALID_ARG for a
+ * pattern outside 0..2, warps outside 1..8, iterations < 1 or a null or short
+ * sink. */
+int gdr_probe_fma(int32_t pattern, int32_t warps_per_subpartition, int32_t iterations, float *sink,
+                  int64_t sink_elements, int32_t *ctas, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -354,3 +354,14 @@ def test_fwd_host_noalloc_rejects_bad_arguments(lib):
     assert call(a) == B.GDR_ERR_UNSUPPORTED
     assert b"staging" in lib.gdr_last_error()
 
+
+
+def test_probe_fma_rejects_bad_arguments(lib):
+    """The diagnostic probe checks its arguments before any CUDA call."""
+    n = ctypes.c_int32(0)
+    fake = 0x7f0000000000
+    for pattern, warps, iters, sink, ctas in [(3, 1, 1, fake, ctypes.byref(n)), (-1, 1, 1, fake, ctypes.byref(n)),
+                                              (0, 0, 1, fake, ctypes.byref(n)), (0, 9, 1, fake, ctypes.byref(n)),
+                                              (0, 1, 0, fake, ctypes.byref(n)), (0, 1, 1, None, ctypes.byref(n)),
+                                              (0, 1, 1, fake, None)]:
+        assert lib.gdr_probe_fma(pattern, warps, iters, sink, 1 << 20, ctas, None) == B.GDR_ERR_INVALID_ARG

@@ -136,24 +136,6 @@ template <int RG, int C> struct LaneState<RG, C, true> {
         }
     }
 
-    // S <- k^ u^T + alpha S.
-    __device__ __forceinline__ void advance(const float *kv, const float (&u)[C], float alpha) {
-        const float2 aa = make_float2(alpha, alpha);
-        float2 uu[C];
-#pragma unroll
-        for (int c = 0; c < C; ++c) uu[c] = make_float2(u[c], u[c]);
-#pragma unroll
-        for (int gp = 0; gp < NP; ++gp) {
-            float2 kp[8];
-            pairs(kv, gp, kp);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-#pragma unroll
-                for (int c = 0; c < C; ++c) x[gp][i][c] = __ffma2_rn(kp[i], uu[c], __fmul2_rn(aa, x[gp][i][c]));
-            }
-        }
-    }
-
     // advance with kc, then partials of the next token (kn, qn) on the new state,
     // in one sweep.
     __device__ __forceinline__ void advance_partials(const float *kc, const float *kn, const float *qn,
